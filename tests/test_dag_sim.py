@@ -1,0 +1,129 @@
+"""Pins for the schedule definitions and the DAG simulator (CPU only).
+
+The closed forms are those printed in DASH overview (zskr.cn) section 3 for m
+heads on n SMs; the cyclic order is the one printed in its section 3.2.
+"""
+import os
+
+import pytest
+
+from oracle import dag_sim as d
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+COSTS = [(3, 1), (1, 1), (5, 2), (7, 1), (4, 1)]
+
+
+def makespan(mode, m, n, causal, P, c, r):
+    return d.simulate(d.all_chains(mode, m, n, causal), P, c, r, ordered=(mode != "atomic")).makespan
+
+
+@pytest.mark.parametrize("n", [4, 8, 16])
+@pytest.mark.parametrize("m", [2, 4, 6])
+@pytest.mark.parametrize("c,r", COSTS)
+def test_closed_forms_at_P_equals_n(n, m, c, r):
+    assert makespan("serial", m, n, True, n, c, r) == d.t_causal_serial(m, n, c, r)
+    assert makespan("shift", m, n, False, n, c, r) == d.t_full_opt(m, n, c, r)
+    assert makespan("symmetric_shift", m, n, True, n, c, r) == d.t_causal_opt(m, n, c, r)
+    # written with "approximately" on the page; exact under the model when c >= r
+    assert makespan("descending_q", m, n, True, n, c, r) == d.t_reversed(m, n, c, r)
+
+
+@pytest.mark.parametrize("n,m,c,r", [(4, 4, 1, 3), (8, 2, 1, 2), (4, 2, 1, 5)])
+def test_descending_formula_is_a_lower_bound_when_r_exceeds_c(n, m, c, r):
+    assert makespan("descending_q", m, n, True, n, c, r) >= d.t_reversed(m, n, c, r)
+
+
+def test_shift_order_matches_printed_cycle():
+    rows = [list(map(int, ln.split())) for ln in open(os.path.join(GOLDEN, "shift_order_n4.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    chains = d.head_chains("shift", 4, False)
+    assert [[q for (kv, q) in ch] for ch in chains] == rows
+    assert [[kv for (kv, q) in ch] for ch in chains] == [[i] * 4 for i in range(4)]
+
+
+@pytest.mark.parametrize("n", [2, 4, 6, 8, 16, 32, 128])
+def test_symmetric_shift_covers_causal_triangle_once(n):
+    chains = d.head_chains("symmetric_shift", n, True)
+    assert len(chains) == n // 2
+    assert all(len(ch) == n + 1 for ch in chains)
+    seen = [t for ch in chains for t in ch]
+    assert sorted(seen) == sorted((kv, q) for kv in range(n) for q in range(kv, n))
+    # phase 1 is the dense lower-left block: KV < n/2, Q >= n/2
+    for p, ch in enumerate(chains):
+        assert all(kv == p and q >= n // 2 for kv, q in ch[: n // 2])
+        assert all(kv == n - 1 - p for kv, q in ch[n - p:])
+    d.head_ranks("symmetric_shift", n, True)   # raises if two chains meet a tile at one step
+
+
+@pytest.mark.parametrize("mode,causal", [("atomic", False), ("atomic", True), ("serial", False),
+                                         ("serial", True), ("descending_q", False),
+                                         ("descending_q", True), ("shift", False)])
+@pytest.mark.parametrize("n", [1, 3, 8])
+def test_chains_cover_mask_and_ranks_are_permutations(mode, causal, n):
+    chains = d.head_chains(mode, n, causal)
+    seen = sorted(t for ch in chains for t in ch)
+    want = sorted((kv, q) for kv in range(n) for q in range(n) if (q >= kv or not causal))
+    assert seen == want
+    ranks = d.head_ranks(mode, n, causal, chains)
+    per_q = {}
+    for ch, rk in zip(chains, ranks):
+        assert len({kv for kv, _ in ch}) == 1           # KV-stationary
+        for (kv, q), r in zip(ch, rk):
+            per_q.setdefault(q, []).append(r)
+    for q, rs in per_q.items():
+        assert sorted(rs) == list(range(len(rs)))
+    if mode == "descending_q":
+        assert all([q for _, q in ch] == sorted((q for _, q in ch), reverse=True) for ch in chains)
+
+
+@pytest.mark.parametrize("mode,causal", [("shift", False), ("symmetric_shift", True)])
+@pytest.mark.parametrize("n,m", [(4, 4), (8, 2), (16, 6)])
+def test_lemma1_conflict_free_schedules_never_wait(mode, causal, n, m):
+    # Lemma 1 (gist.science/it, section 2.2 B): ordering edges that go from a
+    # node to one of no smaller depth keep the critical path.  The shift
+    # schedules build such an order, so no R stage ever waits at P = n.
+    sim = d.simulate(d.all_chains(mode, m, n, causal), n, 4, 1)
+    assert all(sim.r_start[t] == sim.c_end[t] for t in sim.c_end)
+    # and every ordered predecessor's R has ended when the successor's C ends
+    chains = d.all_chains(mode, m, n, causal)
+    by_tile = {}
+    for ci, (bh, ch, rk) in enumerate(chains):
+        for st, ((kv, q), rank) in enumerate(zip(ch, rk)):
+            by_tile.setdefault((bh, q), {})[rank] = (ci, st)
+    for tile, mm in by_tile.items():
+        for rank in range(1, len(mm)):
+            assert sim.r_end[mm[rank - 1]] <= sim.c_end[mm[rank]]
+
+
+def test_serial_waits_exist():
+    sim = d.simulate(d.all_chains("serial", 2, 8, True), 8, 4, 1)
+    assert any(sim.r_start[t] > sim.c_end[t] for t in sim.c_end)
+
+
+def test_shift_needs_a_whole_gang():
+    with pytest.raises(d.Deadlock):
+        d.simulate(d.all_chains("shift", 1, 8, False), 4, 4, 1)
+    d.simulate(d.all_chains("serial", 1, 8, False), 4, 4, 1)       # serial does not
+
+
+def test_invalid_modes_rejected():
+    with pytest.raises(d.ScheduleError):
+        d.head_chains("shift", 4, True)
+    with pytest.raises(d.ScheduleError):
+        d.head_chains("symmetric_shift", 4, False)
+    with pytest.raises(d.ScheduleError):
+        d.head_chains("symmetric_shift", 5, True)
+
+
+def test_tables_flags_and_order():
+    tasks, off, ms = d.schedule_tables("symmetric_shift", 3, 4, True, 5)
+    assert off[0] == 0 and off[-1] == len(tasks) == 3 * 10
+    # each chain of symmetric shift holds two KV runs: first/last flags bracket each
+    for s in range(5):
+        run = tasks[off[s]:off[s + 1]]
+        for i, (bh, kv, q, w) in enumerate(run):
+            first = i == 0 or run[i - 1][1] != kv or run[i - 1][0] != bh
+            last = i == len(run) - 1 or run[i + 1][1] != kv or run[i + 1][0] != bh
+            assert bool(w & d.FLAG_FIRST) == first
+            assert bool(w & d.FLAG_LAST) == last
