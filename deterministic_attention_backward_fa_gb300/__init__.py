@@ -1,0 +1,231 @@
+"""Python binding of libdash (deterministic attention backward for GB300 / sm_103a).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  The functions named ``dash_*`` mirror the C ABI in include/dash.h
+one to one and take torch tensors (device tensors unless stated), passing
+their data pointers and the current CUDA stream.  ``attn_fwd`` / ``attn_bwd``
+allocate the outputs for convenience.
+
+The library must be built first (``__graft_entry__.build()`` or
+``python -m deterministic_attention_backward_fa_gb300._build``); importing a
+function without it raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+from . import _build
+
+SCHEDULES = {"atomic": 0, "serial": 1, "descending_q": 2, "shift": 3, "symmetric_shift": 4}
+STATUS = {0: "DASH_OK", 1: "DASH_ERR_INVALID_ARG", 2: "DASH_ERR_UNSUPPORTED", 3: "DASH_ERR_CUDA",
+          4: "DASH_ERR_TIMEOUT", 5: "DASH_ERR_NO_MEMORY", 6: "DASH_ERR_SCHEDULE"}
+TASK_FIRST = 1 << 28
+TASK_LAST = 1 << 29
+TASK_RANK_MASK = (1 << 24) - 1
+
+# Launches of this library per backward call: preprocess, main, dQ convert.
+KERNELS_PER_BWD = 3
+KERNELS_PER_FWD = 1
+
+
+class DashError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class BwdOptions(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int), ("num_ctas", ctypes.c_int), ("cost_c", ctypes.c_int),
+                ("cost_r", ctypes.c_int), ("spin_limit_ns", ctypes.c_longlong),
+                ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p)]
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+_SIGS = {
+    "dash_attn_fwd": ([_P] * 5 + [_I] * 5 + [_F, _P], _I),
+    "dash_attn_bwd": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
+    "dash_attn_bwd_ex": ([_P] * 9 + [_I] * 5 + [_F, _I, ctypes.POINTER(BwdOptions), _P], _I),
+    "dash_attn_bwd_host": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
+    "dash_schedule_num_tasks": ([_I, _I, _I, _I], ctypes.c_longlong),
+    "dash_build_schedule": ([_I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
+    "dash_choose_ctas": ([_I] * 7, _I),
+    "dash_sync_status": ([_P], _I),
+    "dash_release_workspace": ([], None),
+    "dash_last_error": ([], ctypes.c_char_p),
+    "dash_version": ([], _I),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded libdash.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _LIB = L
+    return _LIB
+
+
+def _check(code: int):
+    if code != 0:
+        raise DashError(code, lib().dash_last_error().decode())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _shape(q: torch.Tensor):
+    if q.dim() != 4:
+        raise ValueError("tensors are [B, H, S, D]")
+    return tuple(int(x) for x in q.shape)
+
+
+def _sched(s) -> int:
+    return SCHEDULES[s] if isinstance(s, str) else int(s)
+
+
+# ------------------------------------------------------------ C mirrors
+def dash_attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
+    B, H, S, D = _shape(q)
+    bf = torch.bfloat16
+    _check(lib().dash_attn_fwd(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+                               _dev(lse, torch.float32, "lse"), B, H, S, D, int(causal), float(scale),
+                               _stream(stream)))
+
+
+def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, stream=None):
+    B, H, S, D = _shape(q)
+    bf = torch.bfloat16
+    _check(lib().dash_attn_bwd(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+                               _dev(do, bf, "do"), _dev(lse, torch.float32, "lse"), _dev(dq, bf, "dq"),
+                               _dev(dk, bf, "dk"), _dev(dv, bf, "dv"), B, H, S, D, int(causal), float(scale),
+                               _sched(schedule), _stream(stream)))
+
+
+def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
+                     num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
+                     cta_off=None, stream=None):
+    B, H, S, D = _shape(q)
+    bf = torch.bfloat16
+    opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None)
+    keep = []
+    if dq_accum_out is not None:
+        opt.dq_accum_out = _dev(dq_accum_out, torch.float32, "dq_accum_out").value
+    if tasks is not None:
+        t = np.ascontiguousarray(tasks, dtype=np.int32)
+        o_ = np.ascontiguousarray(cta_off, dtype=np.int32)
+        keep += [t, o_]
+        opt.tasks = t.ctypes.data
+        opt.cta_off = o_.ctypes.data
+        opt.num_ctas = len(o_) - 1
+    _check(lib().dash_attn_bwd_ex(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+                                  _dev(do, bf, "do"), _dev(lse, torch.float32, "lse"), _dev(dq, bf, "dq"),
+                                  _dev(dk, bf, "dk"), _dev(dv, bf, "dv"), B, H, S, D, int(causal),
+                                  float(scale), _sched(schedule), ctypes.byref(opt), _stream(stream)))
+
+
+def dash_attn_bwd_host(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, stream=None):
+    """All tensors are CPU tensors (pinned for full copy bandwidth); blocks until dq/dk/dv are filled."""
+    B, H, S, D = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do), ("lse", lse), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    _check(lib().dash_attn_bwd_host(*(ctypes.c_void_p(t.data_ptr()) for t in (q, k, v, o, do, lse, dq, dk, dv)),
+                                    B, H, S, D, int(causal), float(scale), _sched(schedule), _stream(stream)))
+
+
+def dash_schedule_num_tasks(BH: int, n: int, causal: bool, schedule) -> int:
+    return int(lib().dash_schedule_num_tasks(BH, n, int(causal), _sched(schedule)))
+
+
+def dash_build_schedule(BH: int, n: int, causal: bool, schedule, P: int, cost_c: int = 4, cost_r: int = 1):
+    """Host-only.  Returns (tasks int32 [N, 4], cta_off int32 [P+1], makespan)."""
+    nt = dash_schedule_num_tasks(BH, n, causal, schedule)
+    if nt < 0:
+        raise DashError(2, "schedule invalid for this mask / n")
+    tasks = np.zeros((max(nt, 1), 4), dtype=np.int32)
+    off = np.zeros(P + 1, dtype=np.int32)
+    ms = ctypes.c_longlong(0)
+    _check(lib().dash_build_schedule(BH, n, int(causal), _sched(schedule), P, cost_c, cost_r,
+                                     tasks.ctypes.data_as(ctypes.c_void_p), off.ctypes.data_as(ctypes.c_void_p),
+                                     ctypes.byref(ms)))
+    return tasks[:nt], off, int(ms.value)
+
+
+def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
+    return int(lib().dash_choose_ctas(BH, n, int(causal), _sched(schedule), max_ctas, cost_c, cost_r))
+
+
+def dash_sync_status(stream=None):
+    _check(lib().dash_sync_status(_stream(stream)))
+
+
+def dash_release_workspace():
+    lib().dash_release_workspace()
+
+
+def dash_last_error() -> str:
+    return lib().dash_last_error().decode()
+
+
+def dash_version() -> int:
+    return int(lib().dash_version())
+
+
+# ------------------------------------------------------------ conveniences
+def attn_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None):
+    """O (bf16) and LSE (fp32, natural log) of softmax attention."""
+    B, H, S, D = _shape(q)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    dash_attn_fwd(q, k, v, o, lse, causal, scale, stream)
+    return o, lse
+
+
+def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None, schedule="serial",
+             dq_accum: bool = False, stream=None, **opts):
+    """dQ, dK, dV (bf16); with ``dq_accum`` also the unscaled fp32 dQ accumulator."""
+    B, H, S, D = _shape(q)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    acc = torch.empty(q.shape, dtype=torch.float32, device=q.device) if dq_accum else None
+    if acc is None and not opts:
+        dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, scale, schedule, stream)
+    else:
+        dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal, scale, schedule, dq_accum_out=acc,
+                         stream=stream, **opts)
+    return (dq, dk, dv, acc) if dq_accum else (dq, dk, dv)

@@ -1,0 +1,482 @@
+// C ABI of the deterministic attention library (declared in include/dash.h).
+//
+// Host side of the backward (DASH overview (zskr.cn), section 2.1; Sintesi
+// Tecnica DASH (gist.science/it), section 1): argument checks, the
+// per-(device, stream) workspace, the cache of schedule tables built by the
+// generator in schedule.cpp, TMA tensor maps, and the three launches
+// (preprocess, persistent main kernel, dQ convert) on the caller's stream.
+#include "dash.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "kernels.h"
+#include "schedule.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dash_status_t fail(dash_status_t code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+dash_status_t cuda_fail(cudaError_t e, const char *what) {
+  return fail(DASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr long long kDefaultSpinNs = 2000000000LL;  // 2 s bound on every device wait
+
+// ------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a contiguous bf16 [BH][S][D] tensor; boxes of 64 columns x box_rows rows.
+dash_status_t make_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(DASH_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DASH_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return DASH_OK;
+}
+
+// ------------------------------------------------------------ workspace
+struct DevBuf {
+  void *ptr = nullptr;
+  size_t bytes = 0;
+  ~DevBuf() {
+    if (ptr) cudaFree(ptr);
+  }
+  cudaError_t reserve(size_t want) {
+    if (want <= bytes) return cudaSuccess;
+    if (ptr) cudaFree(ptr);
+    ptr = nullptr;
+    bytes = 0;
+    cudaError_t e = cudaMalloc(&ptr, want);
+    if (e == cudaSuccess) bytes = want;
+    return e;
+  }
+};
+
+struct Workspace {
+  DevBuf accum, lse2, delta, sem, status;
+  // device copies used by dash_attn_bwd_host
+  DevBuf h_in[6], h_out[3];
+};
+
+struct ScheduleEntry {
+  DevBuf tasks, cta_off;
+  int P = 0;
+  long long makespan = 0;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, void *>, std::unique_ptr<Workspace>> g_ws;
+std::map<std::tuple<int, int, int, int, int, int, int, int>, std::unique_ptr<ScheduleEntry>> g_sched;
+std::map<int, int> g_sms;
+
+int sm_count(int dev) {
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+  g_sms[dev] = n;
+  return n;
+}
+
+Workspace *workspace(int dev, cudaStream_t s) {
+  auto &w = g_ws[{dev, (void *)s}];
+  if (!w) w.reset(new Workspace());
+  return w.get();
+}
+
+cudaError_t ensure_status(Workspace *w) {
+  if (w->status.ptr) return cudaSuccess;
+  cudaError_t e = w->status.reserve(16);
+  if (e == cudaSuccess) e = cudaMemset(w->status.ptr, 0, 16);
+  return e;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dash_status_t check_common(int B, int H, int S, int D, float scale) {
+  if (B < 0 || H < 0 || S < 0) return fail(DASH_ERR_INVALID_ARG, "B, H, S must be >= 0");
+  if (D != 64 && D != 128) return fail(DASH_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", D);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DASH_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if ((long long)B * H > (1LL << 30) || S > (1 << 30)) return fail(DASH_ERR_INVALID_ARG, "problem too large");
+  return DASH_OK;
+}
+
+dash_status_t check_ptrs(std::initializer_list<const void *> ps) {
+  for (const void *p : ps) {
+    if (!p) return fail(DASH_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(p)) return fail(DASH_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  }
+  return DASH_OK;
+}
+
+int auto_tile(int S) { return S <= 256 ? 64 : 128; }
+
+// Checks that a caller-supplied table is in range and that every CTA's list is
+// made of runs on one (head, KV tile) bracketed by the first/last flags.
+dash_status_t validate_table(const int32_t *tasks, const int32_t *off, int P, int BH, int n, bool causal) {
+  if (off[0] != 0) return fail(DASH_ERR_SCHEDULE, "cta_off[0] must be 0");
+  for (int s = 0; s < P; ++s) {
+    if (off[s + 1] < off[s]) return fail(DASH_ERR_SCHEDULE, "cta_off must be non-decreasing");
+    bool in_run = false;
+    int rbh = -1, rkv = -1;
+    for (int t = off[s]; t < off[s + 1]; ++t) {
+      const int32_t *k = tasks + 4 * (size_t)t;
+      const int bh = k[0], kv = k[1], q = k[2], w = k[3];
+      if (bh < 0 || bh >= BH || kv < 0 || kv >= n || q < 0 || q >= n || (causal && q < kv))
+        return fail(DASH_ERR_SCHEDULE, "task %d out of range", t);
+      if ((w & dash::kRankMask) >= n) return fail(DASH_ERR_SCHEDULE, "task %d rank out of range", t);
+      const bool first = w & dash::kTaskFirst, last = w & dash::kTaskLast;
+      if (first == in_run) return fail(DASH_ERR_SCHEDULE, "task %d: runs must start with the first flag", t);
+      if (first) {
+        rbh = bh;
+        rkv = kv;
+      } else if (bh != rbh || kv != rkv) {
+        return fail(DASH_ERR_SCHEDULE, "task %d changes KV tile inside a run", t);
+      }
+      in_run = !last;
+    }
+    if (in_run) return fail(DASH_ERR_SCHEDULE, "CTA %d ends inside a run", s);
+  }
+  return DASH_OK;
+}
+
+dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                       const float *lse, void *dq, void *dk, void *dv, int B, int H, int S, int D, int causal,
+                       float scale, dash_schedule_t schedule, const dash_bwd_options_t *opt,
+                       cudaStream_t stream) {
+  dash_status_t st = check_common(B, H, S, D, scale);
+  if (st != DASH_OK) return st;
+  const int mode = (int)schedule;
+  const int T = (opt && opt->tile) ? opt->tile : auto_tile(S);
+  if (T != 64 && T != 128) return fail(DASH_ERR_UNSUPPORTED, "tile %d not supported (64 or 128)", T);
+  const int BH = B * H;
+  if (BH == 0 || S == 0) return DASH_OK;
+  st = check_ptrs({q, k, v, o, dout, lse, dq, dk, dv});
+  if (st != DASH_OK) return st;
+  if (opt && opt->dq_accum_out && !aligned16(opt->dq_accum_out))
+    return fail(DASH_ERR_INVALID_ARG, "dq_accum_out must be 16-byte aligned");
+  const int n = (S + T - 1) / T;
+  std::string why = dash::check_mode(mode, n, causal != 0);
+  if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  const int c = (opt && opt->cost_c > 0) ? opt->cost_c : 4;
+  const int r = (opt && opt->cost_r > 0) ? opt->cost_r : 1;
+  const long long spin = (opt && opt->spin_limit_ns > 0) ? opt->spin_limit_ns : kDefaultSpinNs;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return fail(DASH_ERR_CUDA, "cannot query the SM count");
+
+  // ---- schedule table (cached per device and problem)
+  const int32_t *dev_tasks = nullptr;
+  const int32_t *dev_off = nullptr;
+  int P = 0;
+  ScheduleEntry custom_holder;  // a caller-supplied table lives for this call only
+  if (opt && opt->tasks) {
+    if (!opt->cta_off || opt->num_ctas < 1) return fail(DASH_ERR_INVALID_ARG, "tasks needs cta_off and num_ctas");
+    P = opt->num_ctas;
+    if (P > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", P, sms);
+    st = validate_table(opt->tasks, opt->cta_off, P, BH, n, causal != 0);
+    if (st != DASH_OK) return st;
+    const size_t nt = (size_t)opt->cta_off[P];
+    if ((e = custom_holder.tasks.reserve(std::max<size_t>(nt, 1) * 16)) != cudaSuccess ||
+        (e = custom_holder.cta_off.reserve((P + 1) * 4)) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc (task table)");
+    if (nt && (e = cudaMemcpy(custom_holder.tasks.ptr, opt->tasks, nt * 16, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy (task table)");
+    if ((e = cudaMemcpy(custom_holder.cta_off.ptr, opt->cta_off, (P + 1) * 4, cudaMemcpyHostToDevice)) !=
+        cudaSuccess)
+      return cuda_fail(e, "cudaMemcpy (task table)");
+    dev_tasks = (const int32_t *)custom_holder.tasks.ptr;
+    dev_off = (const int32_t *)custom_holder.cta_off.ptr;
+  } else {
+    const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
+    if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
+    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r);
+    auto &ent = g_sched[key];
+    if (!ent) {
+      std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
+      const int Puse = want ? want : dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
+      if (Puse < 1) {
+        g_sched.erase(key);
+        return fail(DASH_ERR_UNSUPPORTED, "no CTA count up to %d SMs runs this schedule without deadlock", sms);
+      }
+      dash::Schedule sch;
+      why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch);
+      if (!why.empty()) {
+        g_sched.erase(key);
+        return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+      }
+      if ((e = fresh->tasks.reserve(sch.tasks.size() * 4)) != cudaSuccess ||
+          (e = fresh->cta_off.reserve(sch.cta_off.size() * 4)) != cudaSuccess) {
+        g_sched.erase(key);
+        return cuda_fail(e, "cudaMalloc (schedule)");
+      }
+      cudaMemcpy(fresh->tasks.ptr, sch.tasks.data(), sch.tasks.size() * 4, cudaMemcpyHostToDevice);
+      e = cudaMemcpy(fresh->cta_off.ptr, sch.cta_off.data(), sch.cta_off.size() * 4, cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) {
+        g_sched.erase(key);
+        return cuda_fail(e, "cudaMemcpy (schedule)");
+      }
+      fresh->P = Puse;
+      fresh->makespan = sch.makespan;
+      ent = std::move(fresh);
+    }
+    dev_tasks = (const int32_t *)ent->tasks.ptr;
+    dev_off = (const int32_t *)ent->cta_off.ptr;
+    P = ent->P;
+  }
+
+  // ---- workspace
+  Workspace *w = workspace(dev, stream);
+  const long long rows_padded = (long long)n * T;
+  const long long total_rows = (long long)BH * rows_padded;
+  const long long accum_floats = total_rows * D;
+  if ((e = w->accum.reserve(accum_floats * 4)) != cudaSuccess || (e = w->lse2.reserve(total_rows * 4)) != cudaSuccess ||
+      (e = w->delta.reserve(total_rows * 4)) != cudaSuccess || (e = w->sem.reserve((size_t)BH * n * 4)) != cudaSuccess ||
+      (e = ensure_status(w)) != cudaSuccess)
+    return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
+
+  // ---- tensor maps
+  dash::BwdMaps maps;
+  if ((st = make_map(&maps.q, q, BH, S, D, T)) != DASH_OK) return st;
+  if ((st = make_map(&maps.dout, dout, BH, S, D, T)) != DASH_OK) return st;
+  if ((st = make_map(&maps.k, k, BH, S, D, 128)) != DASH_OK) return st;
+  if ((st = make_map(&maps.v, v, BH, S, D, 128)) != DASH_OK) return st;
+
+  dash::BwdPreParams pre;
+  pre.o = o;
+  pre.dout = dout;
+  pre.lse = lse;
+  pre.lse2 = (float *)w->lse2.ptr;
+  pre.delta = (float *)w->delta.ptr;
+  pre.dq_accum = (float *)w->accum.ptr;
+  pre.accum_floats = accum_floats;
+  pre.sem = (int *)w->sem.ptr;
+  pre.sem_count = BH * n;
+  pre.S = S;
+  pre.D = D;
+  pre.rows_padded = (int)rows_padded;
+  pre.total_rows = total_rows;
+  if ((e = dash::launch_bwd_preprocess(pre, sms, stream)) != cudaSuccess) return cuda_fail(e, "preprocess launch");
+
+  dash::BwdMainParams mp;
+  mp.tasks = (const int4 *)dev_tasks;
+  mp.cta_off = dev_off;
+  mp.lse2 = pre.lse2;
+  mp.delta = pre.delta;
+  mp.dq_accum = pre.dq_accum;
+  mp.sem = pre.sem;
+  mp.dk = (__nv_bfloat16 *)dk;
+  mp.dv = (__nv_bfloat16 *)dv;
+  mp.status = (int *)w->status.ptr;
+  mp.S = S;
+  mp.n = n;
+  mp.scale = scale;
+  mp.scale_log2 = scale * 1.4426950408889634f;
+  mp.causal = causal ? 1 : 0;
+  mp.ordered = mode != DASH_SCHED_ATOMIC;
+  mp.spin_limit_ns = spin;
+  if ((e = dash::launch_bwd_main(D, T, maps, mp, P, stream)) != cudaSuccess) return cuda_fail(e, "main launch");
+  if ((e = dash::launch_bwd_convert(D, T, pre.dq_accum, dq, opt ? opt->dq_accum_out : nullptr, scale, BH, S, n, sms,
+                                    stream)) != cudaSuccess)
+    return cuda_fail(e, "convert launch");
+  return DASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int S,
+                            int D, int causal, float scale, dash_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  dash_status_t st = check_common(B, H, S, D, scale);
+  if (st != DASH_OK) return st;
+  const int BH = B * H;
+  if (BH == 0 || S == 0) return DASH_OK;
+  if ((st = check_ptrs({q, k, v, o, lse})) != DASH_OK) return st;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mu);
+  Workspace *w = workspace(dev, stream);
+  if ((e = ensure_status(w)) != cudaSuccess) return fail(DASH_ERR_NO_MEMORY, "status word allocation failed");
+  CUtensorMap mq, mk, mv;
+  if ((st = make_map(&mq, q, BH, S, D, 128)) != DASH_OK) return st;
+  if ((st = make_map(&mk, k, BH, S, D, 128)) != DASH_OK) return st;
+  if ((st = make_map(&mv, v, BH, S, D, 128)) != DASH_OK) return st;
+  dash::FwdParams p;
+  p.o = (__nv_bfloat16 *)o;
+  p.lse = lse;
+  p.status = (int *)w->status.ptr;
+  p.S = S;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal ? 1 : 0;
+  p.spin_limit_ns = kDefaultSpinNs;
+  if ((e = dash::launch_fwd(D, mq, mk, mv, p, BH, stream)) != cudaSuccess) return cuda_fail(e, "forward launch");
+  return DASH_OK;
+}
+
+dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                            const float *lse, void *dq, void *dk, void *dv, int B, int H, int S, int D, int causal,
+                            float scale, dash_schedule_t schedule, dash_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, schedule, nullptr,
+                  (cudaStream_t)stream);
+}
+
+dash_status_t dash_attn_bwd_ex(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                               const float *lse, void *dq, void *dk, void *dv, int B, int H, int S, int D, int causal,
+                               float scale, dash_schedule_t schedule, const dash_bwd_options_t *opt,
+                               dash_stream_t stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, S, D, causal, scale, schedule, opt,
+                  (cudaStream_t)stream);
+}
+
+dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                                 const float *lse, void *dq, void *dk, void *dv, int B, int H, int S, int D,
+                                 int causal, float scale, dash_schedule_t schedule, dash_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  dash_status_t st = check_common(B, H, S, D, scale);
+  if (st != DASH_OK) return st;
+  if ((long long)B * H * S == 0) return DASH_OK;
+  for (const void *p : {q, k, v, o, dout, (const void *)lse, (const void *)dq, (const void *)dk, (const void *)dv})
+    if (!p) return fail(DASH_ERR_INVALID_ARG, "null pointer");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const size_t tb = (size_t)B * H * S * D * 2, lb = (size_t)B * H * S * 4;
+  void *d[9];
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace *w = workspace(dev, stream);
+    for (int i = 0; i < 6; ++i)
+      if ((e = w->h_in[i].reserve(i == 5 ? lb : tb)) != cudaSuccess)
+        return fail(DASH_ERR_NO_MEMORY, "device input buffers: %s", cudaGetErrorString(e));
+    for (int i = 0; i < 3; ++i)
+      if ((e = w->h_out[i].reserve(tb)) != cudaSuccess)
+        return fail(DASH_ERR_NO_MEMORY, "device output buffers: %s", cudaGetErrorString(e));
+    for (int i = 0; i < 6; ++i) d[i] = w->h_in[i].ptr;
+    for (int i = 0; i < 3; ++i) d[6 + i] = w->h_out[i].ptr;
+  }
+  const void *src[6] = {q, k, v, o, dout, lse};
+  for (int i = 0; i < 6; ++i)
+    if ((e = cudaMemcpyAsync(d[i], src[i], i == 5 ? lb : tb, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpyAsync H2D");
+  st = bwd_impl(d[0], d[1], d[2], d[3], d[4], (const float *)d[5], d[6], d[7], d[8], B, H, S, D, causal, scale,
+                schedule, nullptr, stream);
+  if (st != DASH_OK) return st;
+  void *dst[3] = {dq, dk, dv};
+  for (int i = 0; i < 3; ++i)
+    if ((e = cudaMemcpyAsync(dst[i], d[6 + i], tb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemcpyAsync D2H");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  return dash_sync_status(stream_);
+}
+
+long long dash_schedule_num_tasks(int BH, int n, int causal, dash_schedule_t schedule) {
+  if (BH < 0 || n < 1 || !dash::check_mode((int)schedule, n, causal != 0).empty()) return -1;
+  return dash::num_tasks(BH, n, causal != 0);
+}
+
+dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t schedule, int P, int cost_c, int cost_r,
+                                  int32_t *tasks_out, int32_t *cta_off_out, long long *makespan_out) {
+  if (!tasks_out || !cta_off_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
+  std::string why = dash::check_mode((int)schedule, n, causal != 0);
+  if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  dash::Schedule s;
+  why = dash::build_schedule(BH, n, causal != 0, (int)schedule, P, cost_c, cost_r, &s);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
+  std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
+  if (makespan_out) *makespan_out = s.makespan;
+  return DASH_OK;
+}
+
+int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int cost_c, int cost_r) {
+  return dash::choose_ctas(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r);
+}
+
+dash_status_t dash_sync_status(dash_stream_t stream_) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_ws.find({dev, (void *)stream});
+  if (it == g_ws.end() || !it->second->status.ptr) return DASH_OK;
+  int word = 0;
+  if ((e = cudaMemcpy(&word, it->second->status.ptr, 4, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "reading the status word");
+  if (word == 0) return DASH_OK;
+  const int zero = 0;
+  cudaMemcpy(it->second->status.ptr, &zero, 4, cudaMemcpyHostToDevice);
+  if (word == dash::kStatusSmemMisaligned)
+    return fail(DASH_ERR_CUDA, "device status %d: dynamic shared memory not 1024-byte aligned", word);
+  return fail(DASH_ERR_TIMEOUT, "device status %d: a bounded wait ran out (%s)", word,
+              word == dash::kStatusSemTimeout ? "dQ semaphore" : "mbarrier");
+}
+
+void dash_release_workspace(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return;
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (auto it = g_ws.begin(); it != g_ws.end();)
+    it = (it->first.first == dev) ? g_ws.erase(it) : std::next(it);
+  for (auto it = g_sched.begin(); it != g_sched.end();)
+    it = (std::get<0>(it->first) == dev) ? g_sched.erase(it) : std::next(it);
+}
+
+const char *dash_last_error(void) { return g_last_error.c_str(); }
+
+int dash_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,568 @@
+// Deterministic attention backward for sm_103a.
+//
+// Three kernels run on the caller's stream:
+//   1. dash_bwd_preprocess: delta_i = sum_d dO_id O_id, lse2_i = LSE_i*log2(e)
+//      per query row, and zeroing of the fp32 dQ accumulator and semaphores;
+//   2. dash_bwd_main: persistent, one CTA per schedule slot, walking the task
+//      table that the host generator built.  Each task is one KV tile against
+//      one Q tile.  dK/dV of the CTA's current KV tile accumulate in tensor
+//      memory; the task's dQ partial is added into the accumulator after the
+//      CTA has acquired the tile's semaphore at the task's rank, and the
+//      semaphore is then released at rank + 1 (DASH overview (zskr.cn),
+//      section 2.1: serialised dQ reduction; sections 3.1-3.3: the orders);
+//   3. dash_bwd_convert: dQ = bf16(scale * accumulator).
+//
+// Main-kernel roles (256 threads): warp 0 issues TMA loads, warp 1 owns tensor
+// memory and issues tcgen05 MMAs from one lane, warps 4-7 ("compute", one
+// thread per TMEM lane) do the softmax recompute, dS, the dQ reduction and the
+// dK/dV epilogue.  All MMAs are M = 128: the 128 lanes are KV rows for
+// S^T = K Q^T, dP^T = V dO^T, dV += P^T dO and dK += dS^T Q, and Q rows for
+// dQ = dS K.  With 64-row tiles the KV side is padded to 128 rows (rows past the
+// tile are masked to P = 0) and the Q side of dQ has 64 valid rows.
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace dash {
+
+using namespace dev;
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kComputeWarp0 = 4;
+constexpr int kComputeThreads = 128;
+constexpr int kComputeBar = 1;  // named barrier id of the compute warps
+
+template <int D, int T>
+struct BwdCfg {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kKvRows = 128;
+  static constexpr int kStages = (D == 128 && T == 128) ? 2 : 3;
+  static constexpr uint32_t kKvBytes = kKvRows * D * 2;   // K (and V) tile
+  static constexpr uint32_t kKvPanel = kKvRows * 128;     // bytes per 64-column panel
+  static constexpr uint32_t kQBytes = T * D * 2;          // Q (and dO) tile
+  static constexpr uint32_t kQPanel = T * 128;
+  static constexpr uint32_t kDsBytes = 128 * 128 * 2;     // dS as the A operand of dQ = dS K
+  static constexpr uint32_t kDsPanel = 128 * 128;
+  // shared-memory layout (offsets from a 1024-byte aligned base)
+  static constexpr uint32_t oK = 0;
+  static constexpr uint32_t oV = oK + kKvBytes;
+  static constexpr uint32_t oQ = oV + kKvBytes;
+  static constexpr uint32_t oDO = oQ + kStages * kQBytes;
+  static constexpr uint32_t oDS = oDO + kStages * kQBytes;
+  static constexpr uint32_t oLSE = oDS + kDsBytes;
+  static constexpr uint32_t oDELTA = oLSE + kStages * T * 4;
+  static constexpr uint32_t oBAR = oDELTA + kStages * T * 4;
+  static constexpr int kNumBars = 9 + 2 * kStages;
+  static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = oMISC + 16;
+  // tensor-memory columns
+  static constexpr uint32_t cS = 0, cDP = 128, cDV = 256;
+  static constexpr uint32_t cDK = (D == 128) ? 384 : 320;
+  __host__ __device__ static constexpr uint32_t cDQ(int half) {
+    return D == 128 ? (half == 0 ? 64u : 192u) : 384u;
+  }
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// barrier indices
+enum { bKvFull = 0, bKvEmpty, bSFull, bPdsFull, bDqFull, bTmemFree, bDkvFull, bDkvEmpty, bFinal, bQFull0 };
+
+template <int D, int T>
+__global__ void __launch_bounds__(kThreads, 1)
+    dash_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const BwdMainParams p) {
+  using C = BwdCfg<D, T>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::oBAR);
+  uint64_t *qfull = bars + bQFull0;
+  uint64_t *qempty = bars + bQFull0 + C::kStages;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
+
+  if ((smem_u32(smem) & 1023u) != 0) {  // swizzled operand tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kStatusSmemMisaligned);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[bKvFull], 1);
+    mbar_init(&bars[bKvEmpty], 1);
+    mbar_init(&bars[bSFull], 1);
+    mbar_init(&bars[bPdsFull], 4);
+    mbar_init(&bars[bDqFull], 1);
+    mbar_init(&bars[bTmemFree], 4);
+    mbar_init(&bars[bDkvFull], 1);
+    mbar_init(&bars[bDkvEmpty], 4);
+    mbar_init(&bars[bFinal], 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], 1 + 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+    prefetch_tmap(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Guard g{abort_flag, p.status, (uint64_t)p.spin_limit_ns};
+
+  const int t_begin = p.cta_off[blockIdx.x], t_end = p.cta_off[blockIdx.x + 1];
+  const int4 *tasks = p.tasks;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kv_e_phase = 0;
+      uint32_t qe_phase[C::kStages] = {};
+      uint32_t qf_last[C::kStages] = {};
+      bool q_used[C::kStages] = {};
+      bool kv_issued = false;
+      uint32_t kv_last = 0, kv_fills = 0;
+      int st = 0, runs = 0;
+      for (int t = t_begin; t < t_end; ++t) {
+        const int4 tk = tasks[t];
+        const int bh = tk.x, kv = tk.y, q = tk.z;
+        if (tk.w & kTaskFirstFlag) {
+          if (runs > 0) {
+            mbar_wait(&bars[bKvEmpty], kv_e_phase, g);
+            kv_e_phase ^= 1;
+          }
+          ++runs;
+          if (!*g.abort) {
+            mbar_arrive_expect_tx(&bars[bKvFull], 2 * C::kKvBytes);
+            for (int pn = 0; pn < C::kPanels; ++pn) {
+              tma_load_3d(smem + C::oK + pn * C::kKvPanel, &tmK, &bars[bKvFull], pn * 64, kv * T, bh);
+              tma_load_3d(smem + C::oV + pn * C::kKvPanel, &tmV, &bars[bKvFull], pn * 64, kv * T, bh);
+            }
+            kv_issued = true;
+            kv_last = kv_fills & 1;
+            ++kv_fills;
+          }
+        }
+        if (q_used[st]) {
+          mbar_wait(&qempty[st], qe_phase[st], g);
+          qe_phase[st] ^= 1;
+        }
+        if (!*g.abort) {
+          const uint32_t fill = q_used[st] ? (qf_last[st] ^ 1) : 0;
+          mbar_arrive_expect_tx(&qfull[st], 2 * C::kQBytes + 2 * T * 4);
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_load_3d(smem + C::oQ + st * C::kQBytes + pn * C::kQPanel, &tmQ, &qfull[st], pn * 64, q * T, bh);
+            tma_load_3d(smem + C::oDO + st * C::kQBytes + pn * C::kQPanel, &tmDO, &qfull[st], pn * 64, q * T,
+                        bh);
+          }
+          const size_t row0 = ((size_t)bh * p.n + q) * T;
+          bulk_load(smem + C::oLSE + st * T * 4, p.lse2 + row0, T * 4, &qfull[st]);
+          bulk_load(smem + C::oDELTA + st * T * 4, p.delta + row0, T * 4, &qfull[st]);
+          qf_last[st] = fill;
+          q_used[st] = true;
+        }
+        st = (st + 1 == C::kStages) ? 0 : st + 1;
+      }
+      // let copies still in flight land before the CTA exits
+      for (int s = 0; s < C::kStages; ++s)
+        if (q_used[s]) mbar_drain(&qfull[s], qf_last[s], g.limit_ns);
+      if (kv_issued) mbar_drain(&bars[bKvFull], kv_last, g.limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, T, 0, 0);    // S^T, dP^T: K-major A and B
+      constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t idQ = idesc_bf16(128, 64, 1, 1);   // dQ halves: MN-major A and B
+      uint32_t kvf_phase = 0, dkve_phase = 0, pds_phase = 0, tf_phase = 0;
+      uint32_t qf_phase[C::kStages] = {};
+      int st = 0, runs = 0;
+      const uint32_t sK = smem_u32(smem + C::oK), sV = smem_u32(smem + C::oV);
+      const uint32_t sDS = smem_u32(smem + C::oDS);
+      bool issued = false;
+      for (int t = t_begin; t < t_end; ++t) {
+        const int4 tk = tasks[t];
+        const bool first = tk.w & kTaskFirstFlag, last = tk.w & kTaskLastFlag;
+        if (first) {
+          mbar_wait(&bars[bKvFull], kvf_phase, g);
+          kvf_phase ^= 1;
+          if (runs > 0) {
+            mbar_wait(&bars[bDkvEmpty], dkve_phase, g);
+            dkve_phase ^= 1;
+          }
+          ++runs;
+        }
+        mbar_wait(&qfull[st], qf_phase[st], g);
+        qf_phase[st] ^= 1;
+        if (t > t_begin) {
+          mbar_wait(&bars[bTmemFree], tf_phase, g);
+          tf_phase ^= 1;
+        }
+        const uint32_t sQ = smem_u32(smem + C::oQ + st * C::kQBytes);
+        const uint32_t sDO = smem_u32(smem + C::oDO + st * C::kQBytes);
+        if (!*g.abort) {
+          tc_fence_after();
+          // S^T = K Q^T and dP^T = V dO^T (M = 128 KV rows, N = T, K = D)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kKvPanel + (kk & 3) * 32;
+            const uint32_t offq = (kk >> 2) * C::kQPanel + (kk & 3) * 32;
+            mma_ss(tmem + C::cS, sw128_desc(sK + off, 16, 1024), sw128_desc(sQ + offq, 16, 1024), idS, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kKvPanel + (kk & 3) * 32;
+            const uint32_t offq = (kk >> 2) * C::kQPanel + (kk & 3) * 32;
+            mma_ss(tmem + C::cDP, sw128_desc(sV + off, 16, 1024), sw128_desc(sDO + offq, 16, 1024), idS, kk > 0);
+          }
+          tc_commit(&bars[bSFull]);
+          issued = true;
+        }
+        mbar_wait(&bars[bPdsFull], pds_phase, g);
+        pds_phase ^= 1;
+        if (!*g.abort) {
+          tc_fence_after();
+          // dV += P^T dO and dK += dS^T Q (A from TMEM as packed bf16, B MN-major; K = T)
+#pragma unroll
+          for (int kk = 0; kk < T / 16; ++kk) {
+            const uint64_t b = sw128_desc(sDO + kk * 2048, C::kQPanel, 1024);
+            mma_ts(tmem + C::cDV, tmem + C::cS + kk * 8, b, idKV, (!first || kk > 0) ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < T / 16; ++kk) {
+            const uint64_t b = sw128_desc(sQ + kk * 2048, C::kQPanel, 1024);
+            mma_ts(tmem + C::cDK, tmem + C::cDP + kk * 8, b, idKV, (!first || kk > 0) ? 1u : 0u);
+          }
+          // dQ = dS K (M = 128 Q rows, N = 64 per half, K = 128 KV rows)
+#pragma unroll
+          for (int h = 0; h < C::kPanels; ++h) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              mma_ss(tmem + C::cDQ(h), sw128_desc(sDS + kk * 2048, C::kDsPanel, 1024),
+                     sw128_desc(sK + h * C::kKvPanel + kk * 2048, C::kKvPanel, 1024), idQ, kk > 0);
+            }
+          }
+          tc_commit(&bars[bDqFull]);
+          tc_commit(&qempty[st]);
+          if (last) {
+            tc_commit(&bars[bDkvFull]);
+            tc_commit(&bars[bKvEmpty]);
+          }
+        }
+        st = (st + 1 == C::kStages) ? 0 : st + 1;
+      }
+      if (issued) {  // every MMA has completed before tensor memory is released
+        tc_commit(&bars[bFinal]);
+        mbar_drain(&bars[bFinal], 0, g.limit_ns);
+      }
+    }
+  } else if (warp >= kComputeWarp0) {
+    // ------------------------------------------------------------ compute
+    const int sub = warp & 3;                 // TMEM sub-partition of this warp
+    const int L = sub * 32 + lane;            // TMEM lane = KV row (S, dP) or Q row (dQ)
+    const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
+    const bool ordered = p.ordered != 0;
+    uint32_t sf_phase = 0, dq_phase = 0, dkvf_phase = 0;
+    uint32_t qf_phase[C::kStages] = {};
+    int st = 0;
+    uint8_t *sDS = smem + C::oDS;
+    for (int t = t_begin; t < t_end; ++t) {
+      const int4 tk = tasks[t];
+      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
+      const bool last = tk.w & kTaskLastFlag;
+      const float *sL = reinterpret_cast<const float *>(smem + C::oLSE + st * T * 4);
+      const float *sDl = reinterpret_cast<const float *>(smem + C::oDELTA + st * T * 4);
+      mbar_wait(&qfull[st], qf_phase[st], g);
+      qf_phase[st] ^= 1;
+      mbar_wait(&bars[bSFull], sf_phase, g);
+      sf_phase ^= 1;
+      if (!warp_aborted(g)) {
+        tc_fence_after();
+        const int kv_g = kv * T + L;
+        const bool row_ok = (L < T) && (kv_g < p.S);
+        const int qbase = q * T;
+#pragma unroll 1
+        for (int j0 = 0; j0 < T; j0 += 32) {
+          uint32_t s[32], dp[32];
+          tmem_ld32x2(tl + C::cS + j0, tl + C::cDP + j0, s, dp);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qi = j0 + e + u;
+              float pr = ex2(fmaf(__uint_as_float(s[e + u]), p.scale_log2, -sL[qi]));
+              if (!row_ok || (p.causal && qbase + qi < kv_g)) pr = 0.f;
+              pv[u] = pr;
+              dv[u] = pr * (__uint_as_float(dp[e + u]) - sDl[qi]);
+            }
+            pk[e >> 1] = pack_bf16(pv[0], pv[1]);
+            dk[e >> 1] = pack_bf16(dv[0], dv[1]);
+          }
+          tmem_st16(tl + C::cS + (j0 >> 1), pk);
+          tmem_st16(tl + C::cDP + (j0 >> 1), dk);
+          // dS into shared memory as the MN-major A operand of dQ = dS K: [q/64][kv][64 q]
+          uint8_t *rowp = sDS + (j0 >> 6) * C::kDsPanel + L * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int chunk = ((j0 & 63) >> 3) + i;
+            *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (L & 7)) << 4)) =
+                make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+          }
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[bPdsFull]);
+        mbar_arrive(&qempty[st]);  // this warp is done with the stage's LSE / delta
+      }
+      // -------- dQ partial: TMEM -> registers, then the ordered reduction
+      mbar_wait(&bars[bDqFull], dq_phase, g);
+      dq_phase ^= 1;
+      float acc[D];
+      if (!warp_aborted(g)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tl + C::cDQ(c0 >> 6) + (c0 & 63), r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[c0 + e] = __uint_as_float(r[e]);
+        }
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bTmemFree]);
+      int *sem = p.sem + (size_t)bh * p.n + q;
+      if (ordered) {
+        if (threadIdx.x == kComputeWarp0 * 32 && !*g.abort) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(sem) != rank) {
+            if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+              guard_fail(g, kStatusSemTimeout);
+              break;
+            }
+          }
+        }
+        named_bar(kComputeBar, kComputeThreads);
+      }
+      if (!*g.abort && L < T) {
+        float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
+#pragma unroll
+        for (int c = 0; c < D / 4; ++c)
+          red_add_v4(dst + ((size_t)c * T + L) * 4, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+      }
+      if (ordered) {
+        __threadfence();
+        named_bar(kComputeBar, kComputeThreads);
+        if (threadIdx.x == kComputeWarp0 * 32 && !*g.abort) st_release_gpu(sem, rank + 1);
+      }
+      // -------- end of a KV run: dK, dV out of TMEM
+      if (last) {
+        mbar_wait(&bars[bDkvFull], dkvf_phase, g);
+        dkvf_phase ^= 1;
+        if (!warp_aborted(g)) {
+          tc_fence_after();
+          const int kv_g = kv * T + L;
+          const bool row_ok = (L < T) && (kv_g < p.S);
+          __nv_bfloat16 *dv_row = p.dv + ((size_t)bh * p.S + kv_g) * D;
+          __nv_bfloat16 *dk_row = p.dk + ((size_t)bh * p.S + kv_g) * D;
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t a[32], b[32];
+            tmem_ld32x2(tl + C::cDV + c0, tl + C::cDK + c0, a, b);
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint4 va, vb;
+                va.x = pack_bf16(__uint_as_float(a[8 * i + 0]), __uint_as_float(a[8 * i + 1]));
+                va.y = pack_bf16(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3]));
+                va.z = pack_bf16(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5]));
+                va.w = pack_bf16(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7]));
+                const float sc = p.scale;
+                vb.x = pack_bf16(sc * __uint_as_float(b[8 * i + 0]), sc * __uint_as_float(b[8 * i + 1]));
+                vb.y = pack_bf16(sc * __uint_as_float(b[8 * i + 2]), sc * __uint_as_float(b[8 * i + 3]));
+                vb.z = pack_bf16(sc * __uint_as_float(b[8 * i + 4]), sc * __uint_as_float(b[8 * i + 5]));
+                vb.w = pack_bf16(sc * __uint_as_float(b[8 * i + 6]), sc * __uint_as_float(b[8 * i + 7]));
+                *reinterpret_cast<uint4 *>(dv_row + c0 + 8 * i) = va;
+                *reinterpret_cast<uint4 *>(dk_row + c0 + 8 * i) = vb;
+              }
+            }
+          }
+          tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[bDkvEmpty]);
+      }
+      st = (st + 1 == C::kStages) ? 0 : st + 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// delta, lse2 (padded to n*T rows per head) and zeroing of the workspace.
+template <int D>
+__global__ void __launch_bounds__(256) dash_bwd_preprocess(const __nv_bfloat16 *__restrict__ o,
+                                                          const __nv_bfloat16 *__restrict__ dout,
+                                                          const float *__restrict__ lse, float *lse2,
+                                                          float *delta, float4 *dq_accum, long long accum_vec4,
+                                                          int *sem, int sem_count, int S, int rows_padded,
+                                                          long long total_rows) {
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = gtid; i < accum_vec4; i += nthreads) dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long i = gtid; i < sem_count; i += nthreads) sem[i] = 0;
+  // one warp per padded row
+  const int lane = threadIdx.x & 31;
+  const long long gwarp = gtid >> 5, nwarps = nthreads >> 5;
+  constexpr int kPer = D / 32;  // elements per lane
+  for (long long row = gwarp; row < total_rows; row += nwarps) {
+    const long long bh = row / rows_padded;
+    const int r = (int)(row - bh * rows_padded);
+    float dl = 0.f, l2 = __int_as_float(0x7f800000);  // +inf: P = 0 for padded rows
+    if (r < S) {
+      const size_t base = ((size_t)bh * S + r) * D + lane * kPer;
+      float sum = 0.f;
+      if constexpr (kPer == 4) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(o + base);
+        const uint2 b = *reinterpret_cast<const uint2 *>(dout + base);
+        const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+        const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+          sum = fmaf(fa.x, fb.x, sum);
+          sum = fmaf(fa.y, fb.y, sum);
+        }
+      } else {
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + base);
+        const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+        sum = fmaf(fa.x, fb.x, fa.y * fb.y);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      dl = sum;
+      l2 = lse[(size_t)bh * S + r] * 1.4426950408889634f;
+    }
+    if (lane == 0) {
+      delta[row] = dl;
+      lse2[row] = l2;
+    }
+  }
+}
+
+// dQ = bf16(scale * accumulator); optionally the unscaled fp32 accumulator in [BH][S][D].
+template <int D, int T>
+__global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict__ acc, __nv_bfloat16 *dq,
+                                                       float *acc_out, float scale, int S, int n,
+                                                       long long total_vec4) {
+  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  constexpr int kChunks = D / 4;
+  for (long long i = gtid; i < total_vec4; i += nthreads) {
+    // i enumerates (bh, row, chunk) with chunk fastest: output writes are contiguous
+    const int c = (int)(i % kChunks);
+    const long long rowg = i / kChunks;  // bh * S + row
+    const long long bh = rowg / S;
+    const int row = (int)(rowg - bh * S);
+    const int qt = row / T, r = row - qt * T;
+    const float4 v =
+        *reinterpret_cast<const float4 *>(acc + (((size_t)bh * n + qt) * (size_t)(T * D)) + ((size_t)c * T + r) * 4);
+    uint2 outv;
+    outv.x = pack_bf16(scale * v.x, scale * v.y);
+    outv.y = pack_bf16(scale * v.z, scale * v.w);
+    *reinterpret_cast<uint2 *>(dq + (size_t)rowg * D + c * 4) = outv;
+    if (acc_out) *reinterpret_cast<float4 *>(acc_out + (size_t)rowg * D + c * 4) = v;
+  }
+}
+
+template <int D, int T>
+cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_ctas, cudaStream_t stream) {
+  using C = BwdCfg<D, T>;
+  auto kfn = dash_bwd_main<D, T>;
+  const int smem = C::kSmemBytes > (uint32_t)kMinSmemOneCtaPerSm ? (int)C::kSmemBytes : kMinSmemOneCtaPerSm;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: semaphore waits cannot starve
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, maps.q, maps.k, maps.v, maps.dout, p);
+}
+
+}  // namespace
+
+size_t bwd_main_smem_bytes(int D, int T) {
+  if (D == 64 && T == 64) return BwdCfg<64, 64>::kSmemBytes;
+  if (D == 64 && T == 128) return BwdCfg<64, 128>::kSmemBytes;
+  if (D == 128 && T == 64) return BwdCfg<128, 64>::kSmemBytes;
+  if (D == 128 && T == 128) return BwdCfg<128, 128>::kSmemBytes;
+  return 0;
+}
+
+cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream_t stream) {
+  const int blocks = num_sms * 4;
+  if (a.D == 64)
+    dash_bwd_preprocess<64><<<blocks, 256, 0, stream>>>(
+        (const __nv_bfloat16 *)a.o, (const __nv_bfloat16 *)a.dout, a.lse, a.lse2, a.delta, (float4 *)a.dq_accum,
+        a.accum_floats / 4, a.sem, a.sem_count, a.S, a.rows_padded, a.total_rows);
+  else
+    dash_bwd_preprocess<128><<<blocks, 256, 0, stream>>>(
+        (const __nv_bfloat16 *)a.o, (const __nv_bfloat16 *)a.dout, a.lse, a.lse2, a.delta, (float4 *)a.dq_accum,
+        a.accum_floats / 4, a.sem, a.sem_count, a.S, a.rows_padded, a.total_rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
+                            cudaStream_t stream) {
+  if (D == 64 && T == 64) return launch_main_t<64, 64>(maps, p, num_ctas, stream);
+  if (D == 64 && T == 128) return launch_main_t<64, 128>(maps, p, num_ctas, stream);
+  if (D == 128 && T == 64) return launch_main_t<128, 64>(maps, p, num_ctas, stream);
+  if (D == 128 && T == 128) return launch_main_t<128, 128>(maps, p, num_ctas, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_bwd_convert(int D, int T, const float *acc, void *dq, float *acc_out, float scale, int BH,
+                               int S, int n, int num_sms, cudaStream_t stream) {
+  const long long total = (long long)BH * S * (D / 4);
+  const int blocks = num_sms * 4;
+  auto *out = (__nv_bfloat16 *)dq;
+  if (D == 64 && T == 64) dash_bwd_convert<64, 64><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
+  else if (D == 64 && T == 128) dash_bwd_convert<64, 128><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
+  else if (D == 128 && T == 64) dash_bwd_convert<128, 64><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
+  else dash_bwd_convert<128, 128><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
+  return cudaGetLastError();
+}
+
+}  // namespace dash

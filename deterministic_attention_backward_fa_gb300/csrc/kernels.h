@@ -1,0 +1,82 @@
+// Interface between the host API (api.cpp) and the CUDA kernels (bwd.cu, fwd.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace dash {
+
+// Device status word values (first error wins).
+constexpr int kStatusMbarTimeout = 1;     // an mbarrier wait ran out
+constexpr int kStatusSemTimeout = 2;      // a dQ semaphore wait ran out
+constexpr int kStatusSmemMisaligned = 3;  // dynamic shared memory not 1024-byte aligned
+
+// Dynamic shared memory requested by every kernel that allocates all 512
+// tensor-memory columns: two such CTAs never fit on one SM, so no CTA can sit
+// in tcgen05.alloc behind a CTA that is waiting on it.
+constexpr int kMinSmemOneCtaPerSm = 120 * 1024;
+
+constexpr int kTaskFirstFlag = 1 << 28;
+constexpr int kTaskLastFlag = 1 << 29;
+constexpr int kTaskRankMask = (1 << 24) - 1;
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;  // 3-D [BH][S][D] bf16, 128-byte swizzle; Q/dO box T rows, K/V box 128 rows
+};
+
+struct BwdMainParams {
+  const int4 *tasks;     // {bh, kv, q, rank | flags}
+  const int *cta_off;    // gridDim.x + 1
+  const float *lse2;     // [BH][n*T]  LSE * log2(e), +inf on padded rows
+  const float *delta;    // [BH][n*T]  rowsum(dO * O), 0 on padded rows
+  float *dq_accum;       // [BH][n][D/4][T][4] fp32
+  int *sem;              // [BH][n]
+  __nv_bfloat16 *dk;     // [BH][S][D]
+  __nv_bfloat16 *dv;     // [BH][S][D]
+  int *status;           // device status word
+  int S, n;
+  float scale;           // softmax scale (applied to dK in the epilogue)
+  float scale_log2;      // scale * log2(e)
+  int causal;
+  int ordered;           // 0: atomic (unordered) reduction
+  long long spin_limit_ns;
+};
+
+struct BwdPreParams {
+  const void *o, *dout;  // bf16 [BH][S][D]
+  const float *lse;      // [BH][S]
+  float *lse2, *delta;   // [BH][n*T]
+  float *dq_accum;
+  long long accum_floats;
+  int *sem;
+  int sem_count;
+  int S, D, rows_padded;
+  long long total_rows;  // BH * n * T
+};
+
+struct FwdParams {
+  __nv_bfloat16 *o;  // [BH][S][D]
+  float *lse;        // [BH][S]
+  int *status;
+  int S;
+  float scale_log2;
+  int causal;
+  long long spin_limit_ns;
+};
+
+size_t bwd_main_smem_bytes(int D, int T);
+cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_convert(int D, int T, const float *acc, void *dq, float *acc_out, float scale, int BH,
+                               int S, int n, int num_sms, cudaStream_t stream);
+
+// Forward: Q/K/V maps with 128-row boxes.
+cudaError_t launch_fwd(int D, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                       const FwdParams &p, int BH, cudaStream_t stream);
+
+}  // namespace dash

@@ -1,0 +1,290 @@
+// Host schedule generator for the deterministic attention backward.
+//
+// The DASH model (DASH overview (zskr.cn), section 2.2; Sintesi Tecnica DASH
+// (gist.science/it), section 2.1): every piece of work on one KV tile runs back
+// to back on one SM, forming a chain of tasks; a task is a compute stage C
+// (the KV tile against one Q tile) followed by a reduction stage R (adding the
+// task's dQ partial into the dQ tile).  Determinism fixes, per dQ tile, the
+// order of its R stages.  This file builds the chains of each schedule, the
+// rank of every task in its dQ tile's order, and places chains on the
+// persistent CTAs by discrete-event list scheduling:
+//   * chains are taken in (head, slot) order; at time 0 CTAs 0..P-1 take the
+//     first P chains, afterwards a CTA that falls idle at time T takes the next
+//     chain at T, lowest CTA id first among those idle at the same T;
+//   * a task's C lasts c; its R starts once C has ended and (ordered
+//     schedules) once the R of its predecessor in the dQ tile's order has
+//     ended, and lasts r; the CTA stays busy while it waits.
+// The resulting table is also a proof of deadlock freedom: every wait edge of
+// the device execution points to a task that the simulation finished earlier,
+// so the wait graph is acyclic when every CTA is resident.
+//
+// Schedules (DASH overview, sections 3.1-3.3):
+//   serial / atomic:  KV j visits Q tiles ascending (j..n-1 when causal)
+//   descending_q:     KV j visits Q tiles n-1 down to 0 (down to j when causal)
+//   shift (full):     KV j visits Q tiles (j + t) mod n, t = 0..n-1
+//   symmetric shift (causal, n even): slot p < n/2 runs KV p over Q tiles
+//       n/2 + ((p + t) mod n/2) for t < n/2 (dense lower-left rectangle), then
+//       KV p over Q tiles p..n/2-1, then KV n-1-p over Q tiles n-1 down to
+//       n-1-p (the folded triangle)
+// Serial, descending and atomic rank a dQ tile's partials by KV index; the two
+// shift schedules rank them by the step at which their chain reaches the tile
+// (conflict-free: no two chains of a head reach one tile at the same step).
+#include "schedule.h"
+
+#include <algorithm>
+#include <functional>
+#include <queue>
+#include <utility>
+
+namespace dash {
+
+namespace {
+
+struct HeadPlan {
+  // chains of one head, flattened: chain c holds tasks [off[c], off[c+1])
+  std::vector<int> off;
+  std::vector<int> kv, q, rank;
+};
+
+HeadPlan head_plan(int mode, int n, bool causal) {
+  HeadPlan hp;
+  hp.off.push_back(0);
+  auto push = [&](int kv, int q) {
+    hp.kv.push_back(kv);
+    hp.q.push_back(q);
+  };
+  if (mode == kAtomic || mode == kSerial) {
+    for (int j = 0; j < n; ++j) {
+      for (int q = causal ? j : 0; q < n; ++q) push(j, q);
+      hp.off.push_back((int)hp.kv.size());
+    }
+  } else if (mode == kDescendingQ) {
+    for (int j = 0; j < n; ++j) {
+      for (int q = n - 1; q >= (causal ? j : 0); --q) push(j, q);
+      hp.off.push_back((int)hp.kv.size());
+    }
+  } else if (mode == kShift) {
+    for (int j = 0; j < n; ++j) {
+      for (int t = 0; t < n; ++t) push(j, (j + t) % n);
+      hp.off.push_back((int)hp.kv.size());
+    }
+  } else {  // symmetric shift
+    const int h = n / 2;
+    for (int p = 0; p < h; ++p) {
+      for (int t = 0; t < h; ++t) push(p, h + (p + t) % h);
+      for (int q = p; q < h; ++q) push(p, q);
+      for (int i = 0; i <= p; ++i) push(n - 1 - p, n - 1 - i);
+      hp.off.push_back((int)hp.kv.size());
+    }
+  }
+  const int nt = (int)hp.kv.size();
+  hp.rank.assign(nt, 0);
+  if (mode == kShift || mode == kSymmetricShift) {
+    // rank = position of the visiting step among all visits of the tile
+    std::vector<std::vector<std::pair<int, int>>> visits(n);  // (step, task)
+    const int nch = (int)hp.off.size() - 1;
+    for (int c = 0; c < nch; ++c)
+      for (int t = hp.off[c]; t < hp.off[c + 1]; ++t) visits[hp.q[t]].push_back({t - hp.off[c], t});
+    for (int q = 0; q < n; ++q) {
+      auto &v = visits[q];
+      std::sort(v.begin(), v.end());
+      for (size_t i = 0; i < v.size(); ++i) hp.rank[v[i].second] = (int)i;
+    }
+  } else {
+    for (int t = 0; t < nt; ++t) hp.rank[t] = hp.kv[t];
+  }
+  return hp;
+}
+
+// Per-head predecessor of each task in its dQ tile's order (-1 for rank 0).
+std::vector<int> head_pred(const HeadPlan &hp, int n) {
+  const int nt = (int)hp.kv.size();
+  std::vector<std::vector<int>> by_rank(n);
+  for (int t = 0; t < nt; ++t) {
+    auto &v = by_rank[hp.q[t]];
+    if ((int)v.size() <= hp.rank[t]) v.resize(hp.rank[t] + 1, -1);
+    v[hp.rank[t]] = t;
+  }
+  std::vector<int> pred(nt, -1);
+  for (int q = 0; q < n; ++q)
+    for (size_t r = 1; r < by_rank[q].size(); ++r) pred[by_rank[q][r]] = by_rank[q][r - 1];
+  return pred;
+}
+
+struct SimResult {
+  bool deadlock = false;
+  long long makespan = 0;
+  std::vector<std::vector<int>> chains_of_cta;
+};
+
+SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, int P, int c, int r,
+                   bool ordered) {
+  const int cph = (int)hp.off.size() - 1;   // chains per head
+  const int tph = (int)hp.kv.size();        // tasks per head
+  const long long nch = (long long)BH * cph;
+  SimResult res;
+  res.chains_of_cta.assign(P, {});
+  // task id = head * tph + local task
+  std::vector<char> r_done((size_t)BH * tph, 0);
+  std::vector<int> waiter((size_t)BH * tph, -1);
+  std::vector<long long> cta_chain(P, -1);
+  std::vector<int> cta_step(P, 0);
+  std::vector<char> cta_phase(P, 0);  // 'C', 'R', 'W'
+  using Ev = std::pair<long long, int>;
+  std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> heap;
+  long long next = 0;
+  long long waiting = 0;
+
+  auto task_id = [&](long long chain, int step) -> long long {
+    const long long head = chain / cph;
+    const int local_chain = (int)(chain % cph);
+    return head * tph + hp.off[local_chain] + step;
+  };
+  auto chain_len = [&](long long chain) {
+    const int lc = (int)(chain % cph);
+    return hp.off[lc + 1] - hp.off[lc];
+  };
+  auto dispatch = [&](int s, long long T) {
+    const long long ch = next++;
+    cta_chain[s] = ch;
+    cta_step[s] = 0;
+    cta_phase[s] = 'C';
+    res.chains_of_cta[s].push_back((int)ch);
+    heap.push({T + c, s});
+  };
+
+  for (int s = 0; s < P && next < nch; ++s) dispatch(s, 0);
+  std::vector<int> batch, freed;
+  while (!heap.empty()) {
+    const long long T = heap.top().first;
+    batch.clear();
+    freed.clear();
+    while (!heap.empty() && heap.top().first == T) {
+      batch.push_back(heap.top().second);
+      heap.pop();
+    }
+    std::sort(batch.begin(), batch.end());
+    for (int s : batch) {
+      const long long ch = cta_chain[s];
+      const int st = cta_step[s];
+      const long long tid = task_id(ch, st);
+      if (cta_phase[s] == 'C') {
+        long long p = -1;
+        if (ordered) {
+          const int lp = hpred[(size_t)(tid % tph)];
+          if (lp >= 0) p = (tid / tph) * tph + lp;
+        }
+        if (p < 0 || r_done[(size_t)p]) {
+          cta_phase[s] = 'R';
+          heap.push({T + r, s});
+        } else {
+          cta_phase[s] = 'W';
+          waiter[(size_t)p] = s;
+          ++waiting;
+        }
+      } else {  // R finished
+        r_done[(size_t)tid] = 1;
+        const int w = waiter[(size_t)tid];
+        if (w >= 0) {
+          waiter[(size_t)tid] = -1;
+          --waiting;
+          cta_phase[w] = 'R';
+          heap.push({T + r, w});
+        }
+        if (st + 1 < chain_len(ch)) {
+          cta_step[s] = st + 1;
+          cta_phase[s] = 'C';
+          heap.push({T + c, s});
+        } else {
+          res.makespan = std::max(res.makespan, T);
+          cta_chain[s] = -1;
+          cta_phase[s] = 0;
+          freed.push_back(s);
+        }
+      }
+    }
+    std::sort(freed.begin(), freed.end());
+    for (int s : freed)
+      if (next < nch) dispatch(s, T);
+  }
+  res.deadlock = (next < nch) || (waiting > 0);
+  return res;
+}
+
+}  // namespace
+
+std::string check_mode(int mode, int n, bool causal) {
+  if (mode < kAtomic || mode > kSymmetricShift) return "unknown schedule";
+  if (n < 1) return "n must be >= 1";
+  if (mode == kShift && causal) return "shift scheduling is defined for full masks only";
+  if (mode == kSymmetricShift && !causal) return "symmetric shift is defined for causal masks only";
+  if (mode == kSymmetricShift && (n % 2)) return "symmetric shift needs an even number of blocks";
+  return "";
+}
+
+int chains_per_head(int mode, int n) { return mode == kSymmetricShift ? n / 2 : n; }
+
+long long num_tasks(int BH, int n, bool causal) {
+  const long long per = causal ? (long long)n * (n + 1) / 2 : (long long)n * n;
+  return per * BH;
+}
+
+std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
+                           Schedule *out) {
+  std::string e = check_mode(mode, n, causal);
+  if (!e.empty()) return e;
+  if (BH < 1 || P < 1 || c < 1 || r < 1) return "BH, P and the costs must be >= 1";
+  const HeadPlan hp = head_plan(mode, n, causal);
+  const std::vector<int> hpred = head_pred(hp, n);
+  SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic);
+  if (sim.deadlock) return "schedule simulation deadlocked (too few CTAs for the chain gang?)";
+  const int cph = (int)hp.off.size() - 1;
+  out->tasks.clear();
+  out->tasks.reserve((size_t)num_tasks(BH, n, causal) * 4);
+  out->cta_off.assign(1, 0);
+  for (int s = 0; s < P; ++s) {
+    for (int ch : sim.chains_of_cta[s]) {
+      const int bh = ch / cph, lc = ch % cph;
+      const int a = hp.off[lc], b = hp.off[lc + 1];
+      for (int t = a; t < b; ++t) {
+        int32_t w = hp.rank[t];
+        if (t == a || hp.kv[t - 1] != hp.kv[t]) w |= kTaskFirst;
+        if (t == b - 1 || hp.kv[t + 1] != hp.kv[t]) w |= kTaskLast;
+        out->tasks.push_back(bh);
+        out->tasks.push_back(hp.kv[t]);
+        out->tasks.push_back(hp.q[t]);
+        out->tasks.push_back(w);
+      }
+    }
+    out->cta_off.push_back((int32_t)(out->tasks.size() / 4));
+  }
+  out->makespan = sim.makespan;
+  out->P = P;
+  return "";
+}
+
+int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
+  if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1) return -1;
+  const long long nch = (long long)BH * chains_per_head(mode, n);
+  const int gang = chains_per_head(mode, n);
+  std::vector<int> cand;
+  const int top = (int)std::min<long long>(P_max, nch);
+  cand.push_back(top);
+  for (int m = (top / gang) * gang; m >= gang && (int)cand.size() < 16; m -= gang)
+    if (m != top) cand.push_back(m);
+  const HeadPlan hp = head_plan(mode, n, causal);
+  const std::vector<int> hpred = head_pred(hp, n);
+  int best = -1;
+  long long best_ms = 0;
+  for (int P : cand) {
+    SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic);
+    if (sim.deadlock) continue;
+    if (best < 0 || sim.makespan < best_ms || (sim.makespan == best_ms && P < best)) {
+      best = P;
+      best_ms = sim.makespan;
+    }
+  }
+  return best;
+}
+
+}  // namespace dash

@@ -1,0 +1,41 @@
+// Host schedule generator: DASH chains, reduction ranks and list scheduling
+// on P CTAs.  Pure host C++; see schedule.cpp.
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace dash {
+
+enum Mode { kAtomic = 0, kSerial = 1, kDescendingQ = 2, kShift = 3, kSymmetricShift = 4 };
+
+constexpr int32_t kTaskFirst = 1 << 28;
+constexpr int32_t kTaskLast = 1 << 29;
+constexpr int32_t kRankMask = (1 << 24) - 1;
+
+struct Schedule {
+  std::vector<int32_t> tasks;    // 4 per task: bh, kv, q, rank|flags
+  std::vector<int32_t> cta_off;  // P + 1
+  long long makespan = 0;
+  int P = 0;
+};
+
+// Empty string when (mode, n, causal) is a valid combination, else the reason.
+std::string check_mode(int mode, int n, bool causal);
+
+// Number of chains one head contributes (the gang of a cyclic schedule).
+int chains_per_head(int mode, int n);
+
+long long num_tasks(int BH, int n, bool causal);
+
+// Builds chains for BH heads, simulates them on P CTAs with costs (c, r) and
+// fills `out`.  Returns an empty string on success, else the error.
+std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
+                           Schedule *out);
+
+// Candidate CTA counts (P_max and multiples of the gang size up to it, capped
+// at the number of chains), best simulated makespan, ties to fewer CTAs.
+int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
+
+}  // namespace dash

@@ -1,0 +1,171 @@
+/*
+ * dash.h - C ABI of the GB300 (sm_103a) deterministic attention library.
+ *
+ * The library computes softmax attention forward (O, LSE) and, above all, the
+ * attention backward pass (dQ, dK, dV from Q, K, V, O, dO, LSE) with a dQ
+ * reduction whose order is fixed by a schedule, so that every deterministic
+ * schedule returns bit-identical gradients on every run.  The schedules are
+ * those of "DASH: Deterministic Attention Scheduling for High-throughput
+ * Reproducible LLM Training" as presented in the DASH overview (zskr.cn),
+ * sections 2.1-3.3, and Sintesi Tecnica DASH (gist.science/it), sections
+ * 1-2.2.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are contiguous row-major [B][H][S][D] ("BHSD").  q, k, v, o, dout,
+ *    dq, dk, dv are bf16 (IEEE bfloat16, 2 bytes); lse is fp32 [B][H][S],
+ *    natural log with the scale inside: lse_i = log(sum_j exp(scale*q_i.k_j)).
+ *  - Device pointers unless a function says "host".  The caller owns every
+ *    buffer it passes; pointers must be 16-byte aligned.
+ *  - D must be 64 or 128; B, H, S >= 0 (an empty problem is a no-op that
+ *    returns DASH_OK).  S need not be a multiple of the tile: the ragged tail is
+ *    masked.  Causal masking is square and top-left aligned (query i attends
+ *    keys j <= i).  scale must be finite and > 0.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns after enqueueing.  A device-side failure
+ *    (a bounded wait that ran out) is recorded in a status word that
+ *    dash_sync_status() reads.
+ *  - Errors are returned as dash_status_t; no exception crosses the ABI.
+ *    dash_last_error() describes the last failure of the calling thread.
+ *  - The library keeps a per-(device, stream) workspace (fp32 dQ accumulator,
+ *    per-row softmax statistics, semaphores, status word) and a cache of
+ *    schedule tables.  It grows them with cudaMalloc on first use of a larger
+ *    shape; dash_release_workspace() frees them.  Two calls that run
+ *    concurrently on the same stream cannot overlap, so the workspace is never
+ *    shared by concurrent kernels.
+ */
+#ifndef DASH_H_
+#define DASH_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared opaquely so that C callers need no CUDA headers. */
+typedef struct CUstream_st *dash_stream_t;
+
+/* Order in which the backward reduces dQ partials (DASH overview, section 3;
+ * Sintesi Tecnica DASH, section 2.2).  A chain is the list of Q tiles that one
+ * KV tile visits on one CTA; the rank of a task is its position in its dQ
+ * tile's reduction order. */
+typedef enum {
+  DASH_SCHED_ATOMIC = 0,          /* serial chains, unordered fp32 adds: NOT deterministic (reference point) */
+  DASH_SCHED_SERIAL = 1,          /* KV j visits Q tiles ascending; dQ reduced in ascending KV order (FA3's order, overview section 2.1) */
+  DASH_SCHED_DESCENDING_Q = 2,    /* KV j visits Q tiles descending; ascending KV reduction order (overview section 3.1) */
+  DASH_SCHED_SHIFT = 3,           /* full mask only: KV j visits Q tiles (j+t) mod n; reduced in step order (overview section 3.2) */
+  DASH_SCHED_SYMMETRIC_SHIFT = 4  /* causal only, n even: slot p runs KV p then KV n-1-p, dense rectangle then folded triangle (overview section 3.3) */
+} dash_schedule_t;
+
+typedef enum {
+  DASH_OK = 0,
+  DASH_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad scale, misaligned pointer */
+  DASH_ERR_UNSUPPORTED = 2,   /* D not 64/128, schedule invalid for the mask, odd n for symmetric shift, too few SMs */
+  DASH_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message in dash_last_error) */
+  DASH_ERR_TIMEOUT = 4,       /* a bounded device wait ran out (reported by dash_sync_status) */
+  DASH_ERR_NO_MEMORY = 5,     /* workspace allocation failed */
+  DASH_ERR_SCHEDULE = 6       /* the schedule simulation deadlocked or a supplied task table is malformed */
+} dash_status_t;
+
+/* Task-table encoding used by dash_build_schedule and dash_bwd_options_t:
+ * four int32 per task {bh, kv_block, q_block, word} with
+ * word = rank | (first ? DASH_TASK_FIRST : 0) | (last ? DASH_TASK_LAST : 0). */
+#define DASH_TASK_RANK_MASK 0x00FFFFFF
+#define DASH_TASK_FIRST (1 << 28) /* first task of a run on one KV tile: dK/dV accumulators start at zero */
+#define DASH_TASK_LAST (1 << 29)  /* last task of a run on one KV tile: dK/dV are written out */
+
+/* Softmax attention forward (the input side of the backward; the DASH pages
+ * take it as given).  o[b,h,i,:] = sum_j P_ij v[b,h,j,:] with
+ * P_ij = exp(scale*q_i.k_j - lse_i); writes o (bf16) and lse (fp32). */
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int S, int D, int causal, float scale,
+                            dash_stream_t stream);
+
+/* Attention backward (DASH overview, section 2.1; Sintesi Tecnica DASH,
+ * section 1).  With P as above, dP = dO V^T, delta_i = dO_i.O_i,
+ * dS = P*(dP - delta):  dv = P^T dO, dk = scale * dS^T Q, dq = scale * dS K,
+ * written as bf16.  Each KV tile's work stays on one CTA with dK/dV
+ * accumulated in tensor memory; dQ partials are added into an fp32 workspace
+ * in the order `schedule` fixes, enforced by per-dQ-tile semaphores.  Every
+ * schedule except DASH_SCHED_ATOMIC gives bit-identical results run to run. */
+dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse,
+                            void *dq, void *dk, void *dv,
+                            int B, int H, int S, int D, int causal, float scale,
+                            dash_schedule_t schedule, dash_stream_t stream);
+
+/* Options of dash_attn_bwd_ex; zero-initialise and set what you need. */
+typedef struct {
+  int tile;                /* 0 = auto (64 when S <= 256, else 128), or 64 / 128 */
+  int num_ctas;            /* 0 = choose by simulation; else exactly this many persistent CTAs */
+  int cost_c, cost_r;      /* simulator costs used to place chains on CTAs (0 = 4 and 1) */
+  long long spin_limit_ns; /* bound on each device wait (0 = 2 s) */
+  float *dq_accum_out;     /* optional device fp32 [B,H,S,D]: receives the unscaled dQ accumulator */
+  const int32_t *tasks;    /* optional HOST task table that replaces the generated one (testing) */
+  const int32_t *cta_off;  /* with tasks: HOST array of num_ctas+1 offsets into tasks */
+} dash_bwd_options_t;
+
+/* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
+ * bounds-checked on the host (DASH_ERR_SCHEDULE if an index is out of range);
+ * ranks are taken as given, so an inconsistent table makes the device waits
+ * run out, which dash_sync_status() then reports as DASH_ERR_TIMEOUT. */
+dash_status_t dash_attn_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                               const void *dout, const float *lse,
+                               void *dq, void *dk, void *dv,
+                               int B, int H, int S, int D, int causal, float scale,
+                               dash_schedule_t schedule, const dash_bwd_options_t *opt,
+                               dash_stream_t stream);
+
+/* End-to-end backward from HOST buffers: copies the six inputs to the device,
+ * runs dash_attn_bwd on `stream`, copies dq/dk/dv back and synchronises the
+ * stream.  All pointers are host pointers (pinned memory gives full copy
+ * bandwidth).  Device buffers are cached per (device, stream) and reused. */
+dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, const void *o,
+                                 const void *dout, const float *lse,
+                                 void *dq, void *dk, void *dv,
+                                 int B, int H, int S, int D, int causal, float scale,
+                                 dash_schedule_t schedule, dash_stream_t stream);
+
+/* Number of tasks (q-tile x kv-tile pairs) of one problem: BH*n*n for a full
+ * mask, BH*n*(n+1)/2 for a causal one; -1 if the schedule is invalid for the
+ * mask.  Host only. */
+long long dash_schedule_num_tasks(int BH, int n, int causal, dash_schedule_t schedule);
+
+/* Host schedule generator (DASH overview, section 2.2: chains of C and R
+ * stages list-scheduled on SMs).  Builds the chains of `schedule` for BH
+ * heads of n blocks, simulates them on P CTAs with integer costs c (compute)
+ * and r (reduce), and writes the per-CTA task table: tasks_out (4 int32 per
+ * task, dash_schedule_num_tasks entries), cta_off_out (P+1 entries) and the
+ * simulated makespan.  Returns DASH_ERR_SCHEDULE if the simulation
+ * deadlocks (e.g. a shift schedule on fewer CTAs than its gang of chains).
+ * Host only; no GPU needed. */
+dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t schedule, int P,
+                                  int cost_c, int cost_r, int32_t *tasks_out,
+                                  int32_t *cta_off_out, long long *makespan_out);
+
+/* The CTA count the backward uses for a problem when num_ctas = 0: the
+ * candidate (max_ctas, and the multiples of the schedule's gang size up to
+ * it) whose simulated makespan is smallest, ties to fewer CTAs.  Host only. */
+int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas,
+                     int cost_c, int cost_r);
+
+/* Synchronises `stream` and returns the device status of the calling
+ * thread's current device workspace for that stream: DASH_OK, or
+ * DASH_ERR_TIMEOUT if a bounded wait ran out since the last call (the word is
+ * then cleared). */
+dash_status_t dash_sync_status(dash_stream_t stream);
+
+/* Frees the workspaces and cached schedule tables of the current device. */
+void dash_release_workspace(void);
+
+/* Description of the calling thread's last error ("" if none). */
+const char *dash_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int dash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DASH_H_ */

@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+that include/dash.h declares, and its host schedule generator reproduces the
+oracle simulator's tables element by element."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import deterministic_attention_backward_fa_gb300 as dash
+from oracle import dag_sim as d
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dash.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dash_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "dash_attn_bwd" in names and "dash_attn_fwd" in names
+    L = dash.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in dash.__dict__, f"binding lacks {n}"
+
+
+CASES = [(m, c, n, BH, P) for m in d.MODES for c in (False, True) for n in (1, 2, 4, 6, 16)
+         for BH in (1, 3) for P in (1, 4, 16, 152)]
+
+
+@pytest.mark.parametrize("mode,causal,n,BH,P", CASES)
+def test_generator_matches_simulator(mode, causal, n, BH, P):
+    try:
+        d.check_mode(mode, n, causal)
+    except d.ScheduleError:
+        assert dash.dash_schedule_num_tasks(BH, n, causal, mode) == -1
+        with pytest.raises(dash.DashError) as ei:
+            dash.dash_build_schedule(BH, n, causal, mode, P)
+        assert ei.value.code == 2
+        return
+    for c, r in ((4, 1), (1, 3), (7, 2)):
+        try:
+            py = d.schedule_tables(mode, BH, n, causal, P, c, r)
+        except d.Deadlock:
+            with pytest.raises(dash.DashError) as ei:
+                dash.dash_build_schedule(BH, n, causal, mode, P, c, r)
+            assert ei.value.code == 6
+            continue
+        tasks, off, ms = dash.dash_build_schedule(BH, n, causal, mode, P, c, r)
+        np.testing.assert_array_equal(tasks, np.asarray(py[0], dtype=np.int32).reshape(-1, 4))
+        np.testing.assert_array_equal(off, np.asarray(py[1], dtype=np.int32))
+        assert ms == py[2]
+
+
+@pytest.mark.parametrize("BH,n,causal,mode", [(64, 16, True, "symmetric_shift"), (32, 32, False, "shift"),
+                                              (32, 64, True, "descending_q"), (16, 128, True, "serial")])
+def test_generator_matches_simulator_at_full_size(BH, n, causal, mode):
+    py = d.schedule_tables(mode, BH, n, causal, 152)
+    tasks, off, ms = dash.dash_build_schedule(BH, n, causal, mode, 152)
+    np.testing.assert_array_equal(tasks, np.asarray(py[0], dtype=np.int32).reshape(-1, 4))
+    np.testing.assert_array_equal(off, np.asarray(py[1], dtype=np.int32))
+    assert ms == py[2]
+
+
+@pytest.mark.parametrize("BH,n,causal,mode", [(8, 4, False, "shift"), (6, 8, True, "symmetric_shift"),
+                                              (4, 6, True, "descending_q")])
+def test_cta_choice_is_best_simulated(BH, n, causal, mode):
+    P_max = 40
+    chosen = dash.dash_choose_ctas(BH, n, causal, mode, P_max)
+    gang = n // 2 if mode == "symmetric_shift" else n
+    top = min(P_max, BH * gang)
+    cands = [top] + [m for m in range((top // gang) * gang, gang - 1, -gang) if m != top][:15]
+    spans = {}
+    for P in cands:
+        try:
+            spans[P] = d.simulate(d.all_chains(mode, BH, n, causal), P, 4, 1).makespan
+        except d.Deadlock:
+            pass
+    best = min(spans.values())
+    assert chosen == min(P for P, s in spans.items() if s == best)
+
+
+def test_error_codes_without_gpu():
+    # argument checks run before any CUDA call
+    L = dash.lib()
+    import ctypes
+    nul = ctypes.c_void_p(0)
+    assert L.dash_attn_bwd(*([nul] * 9), 1, 1, 128, 96, 0, 0.1, 1, nul) == 2      # D = 96
+    assert L.dash_attn_bwd(*([nul] * 9), 1, 1, 128, 64, 0, -1.0, 1, nul) == 1     # scale <= 0
+    assert L.dash_attn_bwd(*([nul] * 9), -1, 1, 128, 64, 0, 0.1, 1, nul) == 1    # B < 0
+    assert L.dash_attn_bwd(*([nul] * 9), 0, 1, 128, 64, 0, 0.1, 1, nul) == 0     # empty: no-op
+    assert L.dash_attn_fwd(*([nul] * 5), 1, 1, 128, 64, 0, float("nan"), nul) == 1
+    assert "scale" in dash.dash_last_error()
+    assert dash.dash_schedule_num_tasks(2, 8, True, "shift") == -1
+    assert dash.dash_schedule_num_tasks(2, 8, True, "serial") == 2 * 36
+    assert dash.dash_schedule_num_tasks(2, 7, True, "symmetric_shift") == -1
