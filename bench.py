@@ -1,0 +1,337 @@
+#!/usr/bin/env python
+"""Throughput of the deterministic attention backward on GB300.
+
+One step = one dash_attn_bwd call (preprocess, persistent main kernel, dQ
+convert) over the whole workload, inputs resident in HBM, L2 flushed between
+steps.  Every schedule valid for the workload is timed; `value` is the best
+deterministic schedule's TFLOPS (conventional count: 10*B*H*S^2*D for a full
+mask, half of it for a causal one) and the atomic schedule gives the ratio.
+
+    python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (one head
+of the workload per step).  Under torchrun each rank runs an independent
+replica of the workload on its own GPU (there is no data exchange); rank 0
+prints the JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "deterministic attn-bwd TFLOPS & % BF16 peak; ratio vs own atomicAdd bwd"
+DEFAULT_WORKLOAD = "full_s4096_d128"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = ["bwd.cu", "sm103.cuh", "kernels.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "deterministic_attention_backward_fa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return {"bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in (self.out or "").splitlines():
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w, seconds: float):
+    """The fp64 oracle's backward, head by head, until `seconds` have passed."""
+    from oracle import attention as A
+    q, k, v, do = (t.double().numpy() for t in workloads.make_workload_inputs(w))
+    flops_head = w.flops() / (w.B * w.H)
+    done, spent = 0, 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            o, lse = A.forward(q[sl], k[sl], v[sl], w.causal, w.scale)
+            t0 = time.perf_counter()
+            A.backward(q[sl], k[sl], v[sl], o, do[sl], lse, w.causal, w.scale)
+            spent += time.perf_counter() - t0
+            done += 1
+            if spent >= seconds:
+                break
+        if spent >= seconds:
+            break
+    return {"value": done * flops_head / spent / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"fp64 numpy oracle backward on {done} of {w.B * w.H} heads of {w.name} "
+                      f"({spent:.1f} s), O/LSE from the oracle forward outside the timing"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    w = workloads.WORKLOADS[args.workload]
+    from oracle import attention as A
+    q, k, v, do = (t.double().numpy() for t in workloads.make_workload_inputs(w))
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    pre = {}
+    for i in range(args.warmup + args.steps):
+        b, h = heads[i % len(heads)]
+        if (b, h) not in pre:
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            pre[(b, h)] = A.forward(q[sl], k[sl], v[sl], w.causal, w.scale)
+    times = []
+    for i in range(args.warmup + args.steps):
+        b, h = heads[i % len(heads)]
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        o, lse = pre[(b, h)]
+        t0 = time.perf_counter()
+        A.backward(q[sl], k[sl], v[sl], o, do[sl], lse, w.causal, w.scale)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    flops_head = w.flops() / (w.B * w.H)
+    total = sum(times)
+    value = len(times) * flops_head / total / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                       "mask": "causal" if w.causal else "full", "step": "oracle backward of one head"},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"one head of {w.name} per step, fp64 numpy"},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import deterministic_attention_backward_fa_gb300 as dash
+    from deterministic_attention_backward_fa_gb300 import _build
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    dash.lib()
+
+    w = workloads.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local_rank)
+    host = workloads.make_workload_inputs(w)
+    q, k, v, do = (t.to(dev) for t in host)
+    o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
+    dash.dash_sync_status()
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = w.flops()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    gpu_index = local_rank
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local_rank])
+        except (ValueError, IndexError):
+            pass
+
+    results = {}
+    launches = 0
+    with ClockSampler(gpu_index) as clk:
+        for sched in w.schedules:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                    torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for e in evs:
+                for x in e:
+                    x.record(stream)
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile)
+            dash.dash_sync_status()
+            barrier()
+            torch.cuda.synchronize()
+            for i in range(args.steps):
+                flush.fill_(1)   # evict the previous step's working set from L2
+                evs[i][0].record(stream)
+                dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                      main_events=(evs[i][1], evs[i][2]))
+                evs[i][3].record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            dash.dash_sync_status()
+            launches += dash.KERNELS_PER_BWD * args.steps
+            step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
+            main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+            total_s = max_over_ranks(sum(step_ms) / 1e3)
+            results[sched] = {"ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
+                              "tflops": world * flops * args.steps / total_s / 1e12}
+    clocks = clk.summary()
+
+    det = {s: r for s, r in results.items() if s != "atomic"}
+    best = max(det, key=lambda s: det[s]["tflops"])
+    atomic = results.get("atomic")
+    for s, r in results.items():
+        r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
+
+    # end to end through the host-buffer entry point: H2D inputs, backward, D2H gradients
+    pin = [t.pin_memory() for t in host] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]
+    hq, hk, hv, hdo, ho, hl = pin
+    outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
+    for _ in range(max(1, args.warmup)):
+        dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, w.causal, w.scale, best)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, w.causal, w.scale, best)
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ho, hdo, hl))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = flops / (results[best]["main_ms"] / 1e3) / 1e12
+    traffic = None
+    if os.path.exists(PROFILE_TRAFFIC):
+        with open(PROFILE_TRAFFIC) as fh:
+            tr = json.load(fh)
+        ent = tr.get(w.name, {}).get(best)
+        if ent and ent.get("kernel_hash") == kernel_hash():
+            traffic = ent["dram_bytes_per_launch"]
+
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world >= 1:
+            cpu = cpu_baseline(w, args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": results[best]["tflops"], "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": results[best]["ms"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                       "mask": "causal" if w.causal else "full", "tile": w.tile, "schedule": best,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, outside the step events)",
+                       "flops_per_step": flops},
+            "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
+            "ratio_vs_atomic": results[best]["vs_atomic"],
+            "schedules": results,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
+                         "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+            "e2e": {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "api": "dash_attn_bwd_host (pinned host buffers)"},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -324,7 +324,11 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.causal = causal ? 1 : 0;
   mp.ordered = mode != DASH_SCHED_ATOMIC;
   mp.spin_limit_ns = spin;
+  if (opt && opt->main_begin_event && (e = cudaEventRecord((cudaEvent_t)opt->main_begin_event, stream)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
   if ((e = dash::launch_bwd_main(D, T, maps, mp, P, stream)) != cudaSuccess) return cuda_fail(e, "main launch");
+  if (opt && opt->main_end_event && (e = cudaEventRecord((cudaEvent_t)opt->main_end_event, stream)) != cudaSuccess)
+    return cuda_fail(e, "cudaEventRecord");
   if ((e = dash::launch_bwd_convert(D, T, pre.dq_accum, dq, opt ? opt->dq_accum_out : nullptr, scale, BH, S, n, sms,
                                     stream)) != cudaSuccess)
     return cuda_fail(e, "convert launch");

@@ -103,6 +103,8 @@ typedef struct {
   float *dq_accum_out;     /* optional device fp32 [B,H,S,D]: receives the unscaled dQ accumulator */
   const int32_t *tasks;    /* optional HOST task table that replaces the generated one (testing) */
   const int32_t *cta_off;  /* with tasks: HOST array of num_ctas+1 offsets into tasks */
+  void *main_begin_event;  /* optional cudaEvent_t recorded on `stream` just before the main kernel */
+  void *main_end_event;    /* optional cudaEvent_t recorded on `stream` just after it (timing) */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is

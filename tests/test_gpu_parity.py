@@ -1,0 +1,137 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Small and ragged shapes are compared element by element on every output; the
+four large workloads are compared element by element on sampled heads (each
+head is an independent problem the oracle computes whole), with invariants
+of the gradient checked on every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+import deterministic_attention_backward_fa_gb300 as dash
+import workloads
+from oracle import attention as A
+
+from _gpu import LSE_ABS_TOL, Problem, assert_close, err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+SMALL = [
+    # B, H, S, D, causal, tile: several tiles, ragged tails, both head dims and tiles
+    (1, 2, 256, 64, False, 64),
+    (1, 2, 256, 64, True, 64),
+    (1, 2, 512, 128, True, 128),
+    (1, 1, 333, 64, True, 64),
+    (1, 2, 700, 128, True, 128),
+    (1, 2, 700, 128, False, 128),
+    (2, 2, 640, 64, True, 128),
+    (1, 3, 1000, 64, False, 128),
+    (1, 1, 100, 128, True, 128),     # a single ragged tile
+    (1, 1, 1, 64, False, 64),        # one query, one key
+    (1, 2, 192, 128, False, 64),
+]
+
+
+def schedules_for(causal, S, tile):
+    n = (S + tile - 1) // tile
+    out = []
+    for s in workloads.ALL_SCHEDULES:
+        if s == "shift" and causal:
+            continue
+        if s == "symmetric_shift" and (not causal or n % 2):
+            continue
+        out.append(s)
+    return out
+
+
+@pytest.mark.parametrize("B,H,S,D,causal,tile", SMALL)
+def test_forward_and_backward_match_oracle(B, H, S, D, causal, tile):
+    P = Problem(B, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    dash.dash_sync_status()
+    ro, rl = P.oracle_fwd()
+    assert_close("O", o, ro)
+    assert err(lse, rl)[1] <= LSE_ABS_TOL
+    # end to end: oracle forward + backward from the bf16 inputs
+    q, k, v, do = P.f64
+    ref_e2e = A.backward(q, k, v, ro, do, rl, causal, P.scale)
+    # isolated: oracle backward fed the GPU's O and LSE
+    ref_iso = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    for sched in schedules_for(causal, S, tile):
+        dq, dk, dv = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile)
+        dash.dash_sync_status()
+        for name, x, r1, r2 in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref_iso, ref_e2e):
+            assert_close(f"{sched} {name} (isolated)", x, r1)
+            assert_close(f"{sched} {name} (end to end)", x, r2)
+
+
+LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
+
+
+@pytest.mark.parametrize("w", LARGE, ids=[w.name for w in LARGE])
+def test_full_size_sampled_heads(w):
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    heads = sorted({(0, 0), (w.B - 1, w.H - 1)})
+    ref_f = P.oracle_fwd(heads)
+    for (b, h), (ro, rl) in ref_f.items():
+        assert_close(f"O[{b},{h}]", o[b, h], ro)
+        assert err(lse[b, h], rl)[1] <= LSE_ABS_TOL
+    q, k, v, do = P.f64
+    ref_b = {}
+    for (b, h) in heads:
+        ro, rl = ref_f[(b, h)]
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        r = A.backward(q[sl], k[sl], v[sl], ro[None, None], do[sl], rl[None, None], w.causal, P.scale)
+        ref_b[(b, h)] = [x[0, 0] for x in r]
+    for sched in w.schedules:
+        dq, dk, dv = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile)
+        dash.dash_sync_status()
+        for (b, h), refs in ref_b.items():
+            for name, x, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), refs):
+                assert_close(f"{w.name} {sched} {name}[{b},{h}]", x[b, h], r)
+        # invariants on every head: sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i
+        dk32, dv32, do32 = dk.float(), dv.float(), P.do.float()
+        scale_k = dk32.abs().amax(dim=(2, 3)) * w.S ** 0.5
+        assert bool((dk32.sum(2).abs().amax(-1) <= 0.05 * scale_k + 1e-3).all())
+        dvs, dos = dv32.sum(2), do32.sum(2)
+        assert float((dvs - dos).norm() / dos.norm()) < 2e-2
+        assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+
+
+def test_host_buffer_entry_point_matches_device_path():
+    P = Problem(1, 2, 512, 128, True)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, True, P.scale)
+    dq, dk, dv = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, True, P.scale, "descending_q")
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, ho, hdo, hl = (pin(t) for t in (P.q, P.k, P.v, o, P.do, lse))
+    outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
+    dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, True, P.scale, "descending_q")
+    for a, b in zip(outs, (dq, dk, dv)):
+        assert torch.equal(a, b.cpu())
+
+
+def test_invalid_arguments_are_rejected():
+    P = Problem(1, 2, 640, 64, True)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, True, P.scale)
+    with pytest.raises(dash.DashError) as ei:   # n = 5 blocks: odd
+        dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, True, P.scale, "symmetric_shift")
+    assert ei.value.code == 2
+    with pytest.raises(dash.DashError) as ei:
+        dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, True, P.scale, "shift")
+    assert ei.value.code == 2
+    with pytest.raises(dash.DashError) as ei:
+        dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, True, P.scale, "serial", tile=96)
+    assert ei.value.code == 2
+    bad = np.array([[0, 0, 9, 1 << 28 | 1 << 29]], dtype=np.int32)   # q tile out of range
+    with pytest.raises(dash.DashError) as ei:
+        dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, True, P.scale, "serial", tasks=bad, cta_off=[0, 1])
+    assert ei.value.code == 6
