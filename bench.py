@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--schedules", default="", help="comma-separated subset of the workload's schedules")
+    ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
 
 
@@ -237,8 +239,9 @@ def main():
 
     results = {}
     launches = 0
+    scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
     with ClockSampler(gpu_index) as clk:
-        for sched in w.schedules:
+        for sched in scheds:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                     torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
@@ -268,7 +271,7 @@ def main():
                               "tflops": world * flops * args.steps / total_s / 1e12}
     clocks = clk.summary()
 
-    det = {s: r for s, r in results.items() if s != "atomic"}
+    det = {s: r for s, r in results.items() if s != "atomic"} or results
     best = max(det, key=lambda s: det[s]["tflops"])
     atomic = results.get("atomic")
     for s, r in results.items():
@@ -278,9 +281,9 @@ def main():
     pin = [t.pin_memory() for t in host] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]
     hq, hk, hv, hdo, ho, hl = pin
     outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
-    for _ in range(max(1, args.warmup)):
+    for _ in range(0 if args.no_e2e else max(1, args.warmup)):
         dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, w.causal, w.scale, best)
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = 0 if args.no_e2e else max(3, min(args.steps, 20))
     barrier()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -320,7 +323,7 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
                          "peak_source": f"{peak_kind} bf16_tflops (burst)"},
-            "e2e": {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOPS",
+            "e2e": None if not e2e_steps else {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
             "gpu_launches": launches,
