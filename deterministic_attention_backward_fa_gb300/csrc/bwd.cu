@@ -12,13 +12,29 @@
 //      section 2.1: serialised dQ reduction; sections 3.1-3.3: the orders);
 //   3. dash_bwd_convert: dQ = bf16(scale * accumulator).
 //
-// Main-kernel roles (256 threads): warp 0 issues TMA loads, warp 1 owns tensor
-// memory and issues tcgen05 MMAs from one lane, warps 4-7 ("compute", one
-// thread per TMEM lane) do the softmax recompute, dS, the dQ reduction and the
-// dK/dV epilogue.  All MMAs are M = 128: the 128 lanes are KV rows for
-// S^T = K Q^T, dP^T = V dO^T, dV += P^T dO and dK += dS^T Q, and Q rows for
-// dQ = dS K.  With 64-row tiles the KV side is padded to 128 rows (rows past the
-// tile are masked to P = 0) and the Q side of dQ has 64 valid rows.
+// Main-kernel roles (512 threads, four warpgroups):
+//   warp 0       TMA producer (K/V once per KV run, Q/dO/LSE/delta per task)
+//   warp 1       tensor-memory owner and single-lane tcgen05 MMA issuer
+//   warps 4-11   softmax: warp w handles TMEM sub-partition w % 4 (32 KV rows)
+//                and half of the Q columns of S^T / dP^T; recomputes P,
+//                forms dS and writes both back as bf16
+//   warps 12-15  reduction: drain the dQ partial from TMEM into registers,
+//                then (semaphore-ordered) add it into the fp32 accumulator;
+//                at the end of a KV run, write dK and dV
+// The producer/MMA warpgroup gives registers to the reduction warpgroup
+// (setmaxnreg), which holds a whole dQ row (D fp32 values) per thread.
+//
+// All MMAs are M = 128: the lanes are KV rows for S^T = K Q^T, dP^T = V dO^T,
+// dV += P^T dO and dK += dS^T Q, and Q rows for dQ = dS K.  With 64-row tiles
+// the KV side is padded to 128 rows (rows past the tile are masked to P = 0)
+// and the Q side of dQ has 64 valid rows.
+//
+// Tensor memory (512 columns): S^T at 0, dP^T at 128, dV at 256, dK at 256+D.
+// A softmax warp of half h turns its columns [32h + 64c, +32) of S^T and dP^T
+// into packed bf16 P and dS at columns [32h + 16c, +16) of the same regions,
+// i.e. inside columns it has itself already read, so the two halves never
+// race.  P and dS then fill columns 0-63 of their regions; with D = 128, dQ
+// goes to columns 64-127 of both regions (64 output columns each).
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -30,10 +46,18 @@ using namespace dev;
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kComputeWarp0 = 4;
-constexpr int kComputeThreads = 128;
-constexpr int kComputeBar = 1;  // named barrier id of the compute warps
+constexpr int kThreads = 512;
+constexpr int kSoftWarp0 = 4;
+constexpr int kNumSoftWarps = 8;
+constexpr int kRedWarp0 = 12;
+constexpr int kNumRedWarps = 4;
+constexpr int kRedThreads = kNumRedWarps * 32;
+constexpr int kRedBar = 2;            // named barrier of the reduction warps
+constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
+constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
+constexpr int kRegsReduce = 200;      // warpgroup 3 after setmaxnreg.inc
+static_assert(kRegsProducer * 128 + 2 * kRegsLaunch * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
+              "register split exceeds the CTA's allocation");
 
 template <int D, int T>
 struct BwdCfg {
@@ -59,16 +83,23 @@ struct BwdCfg {
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = oMISC + 16;
   // tensor-memory columns
-  static constexpr uint32_t cS = 0, cDP = 128, cDV = 256;
-  static constexpr uint32_t cDK = (D == 128) ? 384 : 320;
+  static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
   __host__ __device__ static constexpr uint32_t cDQ(int half) {
     return D == 128 ? (half == 0 ? 64u : 192u) : 384u;
   }
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kChunks = T / 64;  // 32-column chunks per softmax warp
 };
 
 // barrier indices
 enum { bKvFull = 0, bKvEmpty, bSFull, bPdsFull, bDqFull, bTmemFree, bDkvFull, bDkvEmpty, bFinal, bQFull0 };
+
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+}
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsReduce));
+}
 
 template <int D, int T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -94,15 +125,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[bKvFull], 1);
     mbar_init(&bars[bKvEmpty], 1);
     mbar_init(&bars[bSFull], 1);
-    mbar_init(&bars[bPdsFull], 4);
+    mbar_init(&bars[bPdsFull], kNumSoftWarps);
     mbar_init(&bars[bDqFull], 1);
-    mbar_init(&bars[bTmemFree], 4);
+    mbar_init(&bars[bTmemFree], kNumRedWarps);
     mbar_init(&bars[bDkvFull], 1);
-    mbar_init(&bars[bDkvEmpty], 4);
+    mbar_init(&bars[bDkvEmpty], kNumRedWarps);
     mbar_init(&bars[bFinal], 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], 1 + 4);
+      mbar_init(&qempty[s], 1 + kNumSoftWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -126,9 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_begin = p.cta_off[blockIdx.x], t_end = p.cta_off[blockIdx.x + 1];
   const int4 *tasks = p.tasks;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    regs_dec();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
       uint32_t kv_e_phase = 0;
       uint32_t qe_phase[C::kStages] = {};
       uint32_t qf_last[C::kStages] = {};
@@ -136,8 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool kv_issued = false;
       uint32_t kv_last = 0, kv_fills = 0;
       int st = 0, runs = 0;
+      int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
       for (int t = t_begin; t < t_end; ++t) {
-        const int4 tk = tasks[t];
+        const int4 tk = nxt;
+        if (t + 1 < t_end) nxt = tasks[t + 1];
         const int bh = tk.x, kv = tk.y, q = tk.z;
         if (tk.w & kTaskFirstFlag) {
           if (runs > 0) {
@@ -180,10 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < C::kStages; ++s)
         if (q_used[s]) mbar_drain(&qfull[s], qf_last[s], g.limit_ns);
       if (kv_issued) mbar_drain(&bars[bKvFull], kv_last, g.limit_ns);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idS = idesc_bf16(128, T, 0, 0);    // S^T, dP^T: K-major A and B
       constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, 64, 1, 1);   // dQ halves: MN-major A and B
@@ -192,9 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       int st = 0, runs = 0;
       const uint32_t sK = smem_u32(smem + C::oK), sV = smem_u32(smem + C::oV);
       const uint32_t sDS = smem_u32(smem + C::oDS);
+      uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);  // K-major
+      uint64_t dK_m = sw128_desc(sK, C::kKvPanel, 1024);                          // MN-major
+      uint64_t dDS_m = sw128_desc(sDS, C::kDsPanel, 1024);
       bool issued = false;
+      int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
       for (int t = t_begin; t < t_end; ++t) {
-        const int4 tk = tasks[t];
+        const int4 tk = nxt;
+        if (t + 1 < t_end) nxt = tasks[t + 1];
         const bool first = tk.w & kTaskFirstFlag, last = tk.w & kTaskLastFlag;
         if (first) {
           mbar_wait(&bars[bKvFull], kvf_phase, g);
@@ -213,20 +250,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sQ = smem_u32(smem + C::oQ + st * C::kQBytes);
         const uint32_t sDO = smem_u32(smem + C::oDO + st * C::kQBytes);
+        // keep the per-k-step descriptor sums inside the loop (hoisting all of
+        // them out of it would need more registers than this warp has)
+        asm volatile("" : "+l"(dK_k), "+l"(dV_k), "+l"(dK_m), "+l"(dDS_m));
         if (!*g.abort) {
           tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T (M = 128 KV rows, N = T, K = D)
+          // S^T = K Q^T and dP^T = V dO^T (M = 128 KV rows, N = T, K = D).  A
+          // descriptor plus (byte offset >> 4) addresses the same tile further on.
+          const uint64_t dQk = sw128_desc(sQ, 16, 1024), dDOk = sw128_desc(sDO, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kKvPanel + (kk & 3) * 32;
-            const uint32_t offq = (kk >> 2) * C::kQPanel + (kk & 3) * 32;
-            mma_ss(tmem + C::cS, sw128_desc(sK + off, 16, 1024), sw128_desc(sQ + offq, 16, 1024), idS, kk > 0);
+            const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
+            const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::cS, dK_k + off, dQk + offq, idS, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kKvPanel + (kk & 3) * 32;
-            const uint32_t offq = (kk >> 2) * C::kQPanel + (kk & 3) * 32;
-            mma_ss(tmem + C::cDP, sw128_desc(sV + off, 16, 1024), sw128_desc(sDO + offq, 16, 1024), idS, kk > 0);
+            const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
+            const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::cDP, dV_k + off, dDOk + offq, idS, kk > 0);
           }
           tc_commit(&bars[bSFull]);
           issued = true;
@@ -235,24 +277,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         pds_phase ^= 1;
         if (!*g.abort) {
           tc_fence_after();
-          // dV += P^T dO and dK += dS^T Q (A from TMEM as packed bf16, B MN-major; K = T)
+          const uint64_t dQm = sw128_desc(sQ, C::kQPanel, 1024), dDOm = sw128_desc(sDO, C::kQPanel, 1024);
+          // dV += P^T dO and dK += dS^T Q: A from TMEM (packed bf16), B MN-major, K = T.
+          // k-step (c, h, j) covers Q rows 32h + 64c + 16j, whose P / dS sit at
+          // packed column 32h + 16c + 8j.
 #pragma unroll
-          for (int kk = 0; kk < T / 16; ++kk) {
-            const uint64_t b = sw128_desc(sDO + kk * 2048, C::kQPanel, 1024);
-            mma_ts(tmem + C::cDV, tmem + C::cS + kk * 8, b, idKV, (!first || kk > 0) ? 1u : 0u);
-          }
+          for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
-          for (int kk = 0; kk < T / 16; ++kk) {
-            const uint64_t b = sw128_desc(sQ + kk * 2048, C::kQPanel, 1024);
-            mma_ts(tmem + C::cDK, tmem + C::cDP + kk * 8, b, idKV, (!first || kk > 0) ? 1u : 0u);
-          }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t acol = 32 * h + 16 * c + 8 * j, q0 = 32 * h + 64 * c + 16 * j;
+                const uint32_t acc = (!first || c + h + j > 0) ? 1u : 0u;
+                mma_ts(tmem + C::cDV, tmem + C::cS + acol, dDOm + ((q0 * 128) >> 4), idKV, acc);
+                mma_ts(tmem + C::cDK, tmem + C::cDP + acol, dQm + ((q0 * 128) >> 4), idKV, acc);
+              }
           // dQ = dS K (M = 128 Q rows, N = 64 per half, K = 128 KV rows)
 #pragma unroll
           for (int h = 0; h < C::kPanels; ++h) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              mma_ss(tmem + C::cDQ(h), sw128_desc(sDS + kk * 2048, C::kDsPanel, 1024),
-                     sw128_desc(sK + h * C::kKvPanel + kk * 2048, C::kKvPanel, 1024), idQ, kk > 0);
+              mma_ss(tmem + C::cDQ(h), dDS_m + ((kk * 2048) >> 4),
+                     dK_m + ((h * C::kKvPanel + kk * 2048) >> 4), idQ, kk > 0);
             }
           }
           tc_commit(&bars[bDqFull]);
@@ -269,20 +315,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(&bars[bFinal], 0, g.limit_ns);
       }
     }
-  } else if (warp >= kComputeWarp0) {
-    // ------------------------------------------------------------ compute
-    const int sub = warp & 3;                 // TMEM sub-partition of this warp
-    const int L = sub * 32 + lane;            // TMEM lane = KV row (S, dP) or Q row (dQ)
+  } else if (warp < kRedWarp0) {
+    // ------------------------------------------------------------ softmax
+    const int sub = warp & 3;                 // TMEM sub-partition: KV rows 32*sub ..
+    const int half = (warp - kSoftWarp0) >> 2;
+    const int L = sub * 32 + lane;            // this thread's KV row (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    const bool ordered = p.ordered != 0;
-    uint32_t sf_phase = 0, dq_phase = 0, dkvf_phase = 0;
+    uint32_t sf_phase = 0;
     uint32_t qf_phase[C::kStages] = {};
     int st = 0;
     uint8_t *sDS = smem + C::oDS;
+    int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
     for (int t = t_begin; t < t_end; ++t) {
-      const int4 tk = tasks[t];
-      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
-      const bool last = tk.w & kTaskLastFlag;
+      const int4 tk = nxt;
+      if (t + 1 < t_end) nxt = tasks[t + 1];
+      const int kv = tk.y, q = tk.z;
       const float *sL = reinterpret_cast<const float *>(smem + C::oLSE + st * T * 4);
       const float *sDl = reinterpret_cast<const float *>(smem + C::oDELTA + st * T * 4);
       mbar_wait(&qfull[st], qf_phase[st], g);
@@ -295,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = (L < T) && (kv_g < p.S);
         const int qbase = q * T;
 #pragma unroll 1
-        for (int j0 = 0; j0 < T; j0 += 32) {
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int j0 = 32 * half + 64 * c;       // first Q column of the chunk
+          const uint32_t pcol = 32 * half + 16 * c;  // its packed P / dS column
           uint32_t s[32], dp[32];
           tmem_ld32x2(tl + C::cS + j0, tl + C::cDP + j0, s, dp);
           uint32_t pk[16], dk[16];
@@ -313,8 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[e >> 1] = pack_bf16(pv[0], pv[1]);
             dk[e >> 1] = pack_bf16(dv[0], dv[1]);
           }
-          tmem_st16(tl + C::cS + (j0 >> 1), pk);
-          tmem_st16(tl + C::cDP + (j0 >> 1), dk);
+          tmem_st16(tl + C::cS + pcol, pk);
+          tmem_st16(tl + C::cDP + pcol, dk);
           // dS into shared memory as the MN-major A operand of dQ = dS K: [q/64][kv][64 q]
           uint8_t *rowp = sDS + (j0 >> 6) * C::kDsPanel + L * 128;
 #pragma unroll
@@ -333,6 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bars[bPdsFull]);
         mbar_arrive(&qempty[st]);  // this warp is done with the stage's LSE / delta
       }
+      st = (st + 1 == C::kStages) ? 0 : st + 1;
+    }
+  } else {
+    // ------------------------------------------------------------ reduction + epilogue
+    regs_inc();
+    const int sub = warp & 3;
+    const int L = sub * 32 + lane;            // Q row of dQ, KV row of dK/dV
+    const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
+    const bool ordered = p.ordered != 0;
+    const bool leader = threadIdx.x == kRedWarp0 * 32;
+    uint32_t dq_phase = 0, dkvf_phase = 0;
+    int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
+    for (int t = t_begin; t < t_end; ++t) {
+      const int4 tk = nxt;
+      if (t + 1 < t_end) nxt = tasks[t + 1];
+      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
+      const bool last = tk.w & kTaskLastFlag;
       // -------- dQ partial: TMEM -> registers, then the ordered reduction
       mbar_wait(&bars[bDqFull], dq_phase, g);
       dq_phase ^= 1;
@@ -352,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[bTmemFree]);
       int *sem = p.sem + (size_t)bh * p.n + q;
       if (ordered) {
-        if (threadIdx.x == kComputeWarp0 * 32 && !*g.abort) {
+        if (leader && !*g.abort) {
           const uint64_t t0 = globaltimer_ns();
           while (ld_acquire_gpu(sem) != rank) {
             if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
@@ -361,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_bar(kComputeBar, kComputeThreads);
+        named_bar(kRedBar, kRedThreads);
       }
       if (!*g.abort && L < T) {
         float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
@@ -371,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ordered) {
         __threadfence();
-        named_bar(kComputeBar, kComputeThreads);
-        if (threadIdx.x == kComputeWarp0 * 32 && !*g.abort) st_release_gpu(sem, rank + 1);
+        named_bar(kRedBar, kRedThreads);
+        if (leader && !*g.abort) st_release_gpu(sem, rank + 1);
       }
       // -------- end of a KV run: dK, dV out of TMEM
       if (last) {
@@ -411,7 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[bDkvEmpty]);
       }
-      st = (st + 1 == C::kStages) ? 0 : st + 1;
     }
   }
 
@@ -505,8 +570,14 @@ template <int D, int T>
 cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_ctas, cudaStream_t stream) {
   using C = BwdCfg<D, T>;
   auto kfn = dash_bwd_main<D, T>;
+  // The setmaxnreg split above assumes the CTA is launched with exactly
+  // kRegsLaunch registers per thread; with fewer, an increase could wait forever.
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kfn);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
   const int smem = C::kSmemBytes > (uint32_t)kMinSmemOneCtaPerSm ? (int)C::kSmemBytes : kMinSmemOneCtaPerSm;
-  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
