@@ -56,6 +56,7 @@ _SIGS = {
     "dash_attn_bwd": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_attn_bwd_ex": ([_P] * 9 + [_I] * 5 + [_F, _I, ctypes.POINTER(BwdOptions), _P], _I),
     "dash_attn_bwd_host": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
+    "dash_attn_bwd_noalloc": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_schedule_num_tasks": ([_I, _I, _I, _I], ctypes.c_longlong),
     "dash_build_schedule": ([_I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
@@ -171,6 +172,16 @@ def dash_attn_bwd_host(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: flo
             raise ValueError(f"{name} must be a contiguous CPU tensor")
     _check(lib().dash_attn_bwd_host(*(ctypes.c_void_p(t.data_ptr()) for t in (q, k, v, o, do, lse, dq, dk, dv)),
                                     B, H, S, D, int(causal), float(scale), _sched(schedule), _stream(stream)))
+
+
+def dash_attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, stream=None):
+    """dash_attn_bwd without device allocation (fixed 32 MiB library-owned workspace; synchronises)."""
+    B, H, S, D = _shape(q)
+    bf = torch.bfloat16
+    _check(lib().dash_attn_bwd_noalloc(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+                                       _dev(do, bf, "do"), _dev(lse, torch.float32, "lse"), _dev(dq, bf, "dq"),
+                                       _dev(dk, bf, "dk"), _dev(dv, bf, "dv"), B, H, S, D, int(causal),
+                                       float(scale), _sched(schedule), _stream(stream)))
 
 
 def dash_schedule_num_tasks(BH: int, n: int, causal: bool, schedule) -> int:

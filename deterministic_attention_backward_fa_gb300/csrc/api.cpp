@@ -337,6 +337,11 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
 
 }  // namespace
 
+namespace dash {
+// Lets other translation units of the library report through dash_last_error().
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace dash
+
 extern "C" {
 
 dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int S,

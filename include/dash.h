@@ -128,6 +128,27 @@ dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, co
                                  int B, int H, int S, int D, int causal, float scale,
                                  dash_schedule_t schedule, dash_stream_t stream);
 
+/* dash_attn_bwd without any device allocation.  For callers that must not
+ * call cudaMalloc while they run: a framework whose caching allocator owns all
+ * device memory, a runtime with a fixed memory budget reserved up front, or
+ * code that cannot afford an allocation that may block or fail.  (The DASH
+ * pages have no counterpart; this is a property of this library.)
+ * Same arguments and results as dash_attn_bwd.  The workspace lives in one
+ * fixed 32 MiB array of device memory inside the library, present on every
+ * GPU that loads the library until the process exits; problems whose
+ * workspace does not fit (roughly B*H*S*D above 7.8 M elements) return
+ * DASH_ERR_UNSUPPORTED with the required size in dash_last_error().  The
+ * first call on a device looks up the array's device address (make that
+ * first call before any stream capture).  Every call clears what must start at
+ * zero, but all calls share the array: calls whose GPU work overlaps (other
+ * streams or threads) race on it.  The call synchronises `stream` before it
+ * returns and reports a device wait that ran out as DASH_ERR_TIMEOUT. */
+dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                    const void *dout, const float *lse,
+                                    void *dq, void *dk, void *dv,
+                                    int B, int H, int S, int D, int causal, float scale,
+                                    dash_schedule_t schedule, dash_stream_t stream);
+
 /* Number of tasks (q-tile x kv-tile pairs) of one problem: BH*n*n for a full
  * mask, BH*n*(n+1)/2 for a causal one; -1 if the schedule is invalid for the
  * mask.  Host only. */
