@@ -298,7 +298,11 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   pre.lse2 = (float *)w->lse2.ptr;
   pre.delta = (float *)w->delta.ptr;
   pre.dq_accum = (float *)w->accum.ptr;
-  pre.accum_floats = accum_floats;
+  // Ordered schedules store their rank-0 partial, so the accumulator needs no
+  // zeroing; the atomic schedule (and a caller-supplied table, which need not
+  // hold every rank) adds into zeros.
+  const bool ordered = mode != DASH_SCHED_ATOMIC;
+  pre.accum_floats = (ordered && !(opt && opt->tasks)) ? 0 : accum_floats;
   pre.sem = (int *)w->sem.ptr;
   pre.sem_count = BH * n;
   pre.S = S;

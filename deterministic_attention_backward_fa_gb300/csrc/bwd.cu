@@ -18,11 +18,18 @@
 //   warps 4-11   softmax: warp w handles TMEM sub-partition w % 4 (32 KV rows)
 //                and half of the Q columns of S^T / dP^T; recomputes P,
 //                forms dS and writes both back as bf16
-//   warps 12-15  reduction: drain the dQ partial from TMEM into registers,
-//                then (semaphore-ordered) add it into the fp32 accumulator;
-//                at the end of a KV run, write dK and dV
-// The producer/MMA warpgroup gives registers to the reduction warpgroup
-// (setmaxnreg), which holds a whole dQ row (D fp32 values) per thread.
+//   warps 2, 3   reduce issuers, taking tasks alternately: wait until the
+//                task's dQ partial is staged, acquire the dQ tile's semaphore
+//                at the task's rank, have the TMA engine add the staged tile
+//                into the fp32 accumulator (bulk reduce-add; rank 0 of an
+//                ordered schedule stores instead, so the accumulator needs no
+//                zeroing), hand the stage back to the producer once the TMA
+//                has read it, and release rank + 1 once the add has completed
+//   warps 12-15  reduction: drain the dQ partial from TMEM into shared memory
+//                (the task's own Q + dO stage, which the MMAs no longer read
+//                and which has exactly the size of the fp32 dQ tile); at the
+//                end of a KV run, write dK and dV
+// setmaxnreg gives the softmax warpgroups more registers than the others.
 //
 // All MMAs are M = 128: the lanes are KV rows for S^T = K Q^T, dP^T = V dO^T,
 // dV += P^T dO and dK += dS^T Q, and Q rows for dQ = dS K.  With 64-row tiles
@@ -33,8 +40,14 @@
 // A softmax warp of half h turns its columns [32h + 64c, +32) of S^T and dP^T
 // into packed bf16 P and dS at columns [32h + 16c, +16) of the same regions,
 // i.e. inside columns it has itself already read, so the two halves never
-// race.  P and dS then fill columns 0-63 of their regions; with D = 128, dQ
-// goes to columns 64-127 of both regions (64 output columns each).
+// race.  P and dS then fill columns 0-63 of their regions.  dQ (one N = D
+// MMA) goes to the dP^T region when D = 128 (after dK has read dS there;
+// tcgen05 MMAs of one CTA run in issue order) and to columns 384+ when D = 64.
+//
+// Per task the MMA warp issues S^T, then dP^T; the softmax warps turn S^T into
+// P as soon as S^T is done (pass A) so that dV can start while they form dS
+// from dP^T (pass B); then dK and dQ.  The next task's S^T can be issued right
+// after dQ, while the reduction warps drain dQ; only dP^T waits for that drain.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -51,12 +64,12 @@ constexpr int kSoftWarp0 = 4;
 constexpr int kNumSoftWarps = 8;
 constexpr int kRedWarp0 = 12;
 constexpr int kNumRedWarps = 4;
-constexpr int kRedThreads = kNumRedWarps * 32;
-constexpr int kRedBar = 2;            // named barrier of the reduction warps
 constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
 constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
-constexpr int kRegsReduce = 200;      // warpgroup 3 after setmaxnreg.inc
-static_assert(kRegsProducer * 128 + 2 * kRegsLaunch * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
+constexpr int kRegsSoftmax = 144;     // warpgroups 1, 2 after setmaxnreg.inc
+static_assert(kRegsProducer < kRegsLaunch, "warpgroup 0 must give registers up before the others take them");
+constexpr int kRegsReduce = 136;      // warpgroup 3 after setmaxnreg.inc
+static_assert(kRegsProducer * 128 + 2 * kRegsSoftmax * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
               "register split exceeds the CTA's allocation");
 
 template <int D, int T>
@@ -79,27 +92,37 @@ struct BwdCfg {
   static constexpr uint32_t oLSE = oDS + kDsBytes;
   static constexpr uint32_t oDELTA = oLSE + kStages * T * 4;
   static constexpr uint32_t oBAR = oDELTA + kStages * T * 4;
-  static constexpr int kNumBars = 9 + 2 * kStages;
+  static constexpr int kNumBars = 11 + 3 * kStages;
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = oMISC + 16;
   // tensor-memory columns
   static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
-  __host__ __device__ static constexpr uint32_t cDQ(int half) {
-    return D == 128 ? (half == 0 ? 64u : 192u) : 384u;
-  }
+  static constexpr uint32_t cDQ = (D == 128) ? 128u : 384u;
+  static constexpr bool kDqInDp = (D == 128);  // dQ reuses the dP^T columns
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kChunks = T / 64;  // 32-column chunks per softmax warp
 };
 
 // barrier indices
-enum { bKvFull = 0, bKvEmpty, bSFull, bPdsFull, bDqFull, bTmemFree, bDkvFull, bDkvEmpty, bFinal, bQFull0 };
+enum {
+  bKvFull = 0, bKvEmpty, bSFull, bDpFull, bPFull, bDsFull, bDqFull, bTmemFree, bDkvFull, bDkvEmpty, bFinal, bQFull0
+};
 
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+// setmaxnreg towards N registers per thread: .inc may only raise and .dec only
+// lower the warpgroup's count (which starts at kRegsLaunch), so the direction
+// follows from N.
+template <int N>
+__device__ __forceinline__ void regs_set() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg takes a multiple of 8 in [24, 256]");
+  if constexpr (N > kRegsLaunch) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  } else if constexpr (N < kRegsLaunch) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+  }
 }
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsReduce));
-}
+__device__ __forceinline__ void regs_dec() { regs_set<kRegsProducer>(); }
+__device__ __forceinline__ void regs_softmax() { regs_set<kRegsSoftmax>(); }
+__device__ __forceinline__ void regs_reduce() { regs_set<kRegsReduce>(); }
 
 template <int D, int T>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -114,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::oBAR);
   uint64_t *qfull = bars + bQFull0;
   uint64_t *qempty = bars + bQFull0 + C::kStages;
+  uint64_t *staged = bars + bQFull0 + 2 * C::kStages;  // dQ partial of the stage's task is in smem
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
 
@@ -125,7 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[bKvFull], 1);
     mbar_init(&bars[bKvEmpty], 1);
     mbar_init(&bars[bSFull], 1);
-    mbar_init(&bars[bPdsFull], kNumSoftWarps);
+    mbar_init(&bars[bDpFull], 1);
+    mbar_init(&bars[bPFull], kNumSoftWarps);
+    mbar_init(&bars[bDsFull], kNumSoftWarps);
     mbar_init(&bars[bDqFull], 1);
     mbar_init(&bars[bTmemFree], kNumRedWarps);
     mbar_init(&bars[bDkvFull], 1);
@@ -134,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&qfull[s], 1);
       mbar_init(&qempty[s], 1 + kNumSoftWarps);
+      mbar_init(&staged[s], kNumRedWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -214,12 +241,57 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < C::kStages; ++s)
         if (q_used[s]) mbar_drain(&qfull[s], qf_last[s], g.limit_ns);
       if (kv_issued) mbar_drain(&bars[bKvFull], kv_last, g.limit_ns);
+    } else if ((warp == 2 || warp == 3) && lane == 0) {
+      // ------------------------------------------------------------ reduce issuers
+      const bool ordered = p.ordered != 0;
+      const int mine = warp - 2;
+      for (int t = t_begin + mine; t < t_end; t += 2) {
+        const int i = t - t_begin;
+        const int st = i % C::kStages;
+        const int4 tk = tasks[t];
+        const int bh = tk.x, q = tk.z, rank = tk.w & kTaskRankMask;
+        uint8_t *stage0 = smem + C::oQ + st * C::kQBytes;
+        uint8_t *stage1 = smem + C::oDO + st * C::kQBytes;
+        mbar_wait(&staged[st], (uint32_t)((i / C::kStages) & 1), g);
+        int *sem = p.sem + (size_t)bh * p.n + q;
+        if (ordered && !*g.abort) {
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(sem) != rank) {
+            if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+              guard_fail(g, kStatusSemTimeout);
+              break;
+            }
+          }
+        }
+        const bool go = !*g.abort;
+        if (go) {
+          float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
+          fence_proxy_async_global();
+          if (ordered && rank == 0) {  // first in the tile's order: store
+            bulk_store(dst, stage0, C::kQBytes);
+            bulk_store(dst + C::kQBytes / 4, stage1, C::kQBytes);
+          } else {
+            bulk_reduce_add_f32(dst, stage0, C::kQBytes);
+            bulk_reduce_add_f32(dst + C::kQBytes / 4, stage1, C::kQBytes);
+          }
+          bulk_commit();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&qempty[st]);  // the stage may be refilled
+        if (go) {
+          bulk_wait_all();  // the add has been performed in L2
+          if (ordered) {
+            fence_proxy_async_global();
+            st_release_gpu(sem, rank + 1);  // release: the next rank's acquire sees the sum
+          }
+        }
+      }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idS = idesc_bf16(128, T, 0, 0);    // S^T, dP^T: K-major A and B
       constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
-      constexpr uint32_t idQ = idesc_bf16(128, 64, 1, 1);   // dQ halves: MN-major A and B
-      uint32_t kvf_phase = 0, dkve_phase = 0, pds_phase = 0, tf_phase = 0;
+      constexpr uint32_t idQ = idesc_bf16(128, D, 1, 1);    // dQ: MN-major A and B
+      uint32_t kvf_phase = 0, dkve_phase = 0, pf_phase = 0, dsf_phase = 0, tf_phase = 0;
       uint32_t qf_phase[C::kStages] = {};
       int st = 0, runs = 0;
       const uint32_t sK = smem_u32(smem + C::oK), sV = smem_u32(smem + C::oV);
@@ -244,10 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_wait(&qfull[st], qf_phase[st], g);
         qf_phase[st] ^= 1;
-        if (t > t_begin) {
-          mbar_wait(&bars[bTmemFree], tf_phase, g);
-          tf_phase ^= 1;
-        }
         const uint32_t sQ = smem_u32(smem + C::oQ + st * C::kQBytes);
         const uint32_t sDO = smem_u32(smem + C::oDO + st * C::kQBytes);
         // keep the per-k-step descriptor sums inside the loop (hoisting all of
@@ -255,32 +323,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("" : "+l"(dK_k), "+l"(dV_k), "+l"(dK_m), "+l"(dDS_m));
         if (!*g.abort) {
           tc_fence_after();
-          // S^T = K Q^T and dP^T = V dO^T (M = 128 KV rows, N = T, K = D).  A
-          // descriptor plus (byte offset >> 4) addresses the same tile further on.
-          const uint64_t dQk = sw128_desc(sQ, 16, 1024), dDOk = sw128_desc(sDO, 16, 1024);
+          // S^T = K Q^T (M = 128 KV rows, N = T, K = D).  A descriptor plus
+          // (byte offset >> 4) addresses the same tile further on.
+          const uint64_t dQk = sw128_desc(sQ, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
             const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
             mma_ss(tmem + C::cS, dK_k + off, dQk + offq, idS, kk > 0);
           }
+          tc_commit(&bars[bSFull]);
+          issued = true;
+        }
+        if (C::kDqInDp && t > t_begin) {  // the previous dQ sits in the dP^T columns
+          mbar_wait(&bars[bTmemFree], tf_phase, g);
+          tf_phase ^= 1;
+        }
+        if (!*g.abort) {
+          tc_fence_after();
+          // dP^T = V dO^T
+          const uint64_t dDOk = sw128_desc(sDO, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
             const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
             mma_ss(tmem + C::cDP, dV_k + off, dDOk + offq, idS, kk > 0);
           }
-          tc_commit(&bars[bSFull]);
-          issued = true;
+          tc_commit(&bars[bDpFull]);
         }
-        mbar_wait(&bars[bPdsFull], pds_phase, g);
-        pds_phase ^= 1;
+        mbar_wait(&bars[bPFull], pf_phase, g);
+        pf_phase ^= 1;
+        const uint64_t dQm = sw128_desc(sQ, C::kQPanel, 1024), dDOm = sw128_desc(sDO, C::kQPanel, 1024);
         if (!*g.abort) {
           tc_fence_after();
-          const uint64_t dQm = sw128_desc(sQ, C::kQPanel, 1024), dDOm = sw128_desc(sDO, C::kQPanel, 1024);
-          // dV += P^T dO and dK += dS^T Q: A from TMEM (packed bf16), B MN-major, K = T.
-          // k-step (c, h, j) covers Q rows 32h + 64c + 16j, whose P / dS sit at
-          // packed column 32h + 16c + 8j.
+          // dV += P^T dO: A from TMEM (packed bf16), B MN-major, K = T.  k-step
+          // (c, h, j) covers Q rows 32h + 64c + 16j, whose P sits at packed
+          // column 32h + 16c + 8j.
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
@@ -288,21 +366,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
                 const uint32_t acol = 32 * h + 16 * c + 8 * j, q0 = 32 * h + 64 * c + 16 * j;
-                const uint32_t acc = (!first || c + h + j > 0) ? 1u : 0u;
-                mma_ts(tmem + C::cDV, tmem + C::cS + acol, dDOm + ((q0 * 128) >> 4), idKV, acc);
-                mma_ts(tmem + C::cDK, tmem + C::cDP + acol, dQm + ((q0 * 128) >> 4), idKV, acc);
+                mma_ts(tmem + C::cDV, tmem + C::cS + acol, dDOm + ((q0 * 128) >> 4), idKV,
+                       (!first || c + h + j > 0) ? 1u : 0u);
               }
-          // dQ = dS K (M = 128 Q rows, N = 64 per half, K = 128 KV rows)
+        }
+        mbar_wait(&bars[bDsFull], dsf_phase, g);
+        dsf_phase ^= 1;
+        if (!C::kDqInDp && t > t_begin) {
+          mbar_wait(&bars[bTmemFree], tf_phase, g);
+          tf_phase ^= 1;
+        }
+        if (!*g.abort) {
+          tc_fence_after();
+          // dK += dS^T Q, same k-step order as dV
 #pragma unroll
-          for (int h = 0; h < C::kPanels; ++h) {
+          for (int c = 0; c < C::kChunks; ++c)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              mma_ss(tmem + C::cDQ(h), dDS_m + ((kk * 2048) >> 4),
-                     dK_m + ((h * C::kKvPanel + kk * 2048) >> 4), idQ, kk > 0);
-            }
-          }
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+                const uint32_t acol = 32 * h + 16 * c + 8 * j, q0 = 32 * h + 64 * c + 16 * j;
+                mma_ts(tmem + C::cDK, tmem + C::cDP + acol, dQm + ((q0 * 128) >> 4), idKV,
+                       (!first || c + h + j > 0) ? 1u : 0u);
+              }
+          // dQ = dS K (M = 128 Q rows, N = D, K = 128 KV rows)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + C::cDQ, dDS_m + ((kk * 2048) >> 4), dK_m + ((kk * 2048) >> 4), idQ, kk > 0);
           tc_commit(&bars[bDqFull]);
-          tc_commit(&qempty[st]);
           if (last) {
             tc_commit(&bars[bDkvFull]);
             tc_commit(&bars[bKvEmpty]);
@@ -317,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kRedWarp0) {
     // ------------------------------------------------------------ softmax
+    regs_softmax();
     const int sub = warp & 3;                 // TMEM sub-partition: KV rows 32*sub ..
     const int half = (warp - kSoftWarp0) >> 2;
     const int L = sub * 32 + lane;            // this thread's KV row (TMEM lane)
@@ -335,42 +427,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&qfull[st], qf_phase[st], g);
       qf_phase[st] ^= 1;
       mbar_wait(&bars[bSFull], sf_phase, g);
-      sf_phase ^= 1;
+      float pv[C::kChunks][32];  // P of this thread's row and columns, kept for pass B
       if (!warp_aborted(g)) {
         tc_fence_after();
         const int kv_g = kv * T + L;
         const bool row_ok = (L < T) && (kv_g < p.S);
         const int qbase = q * T;
-#pragma unroll 1
+        // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns
+#pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          const int j0 = 32 * half + 64 * c;       // first Q column of the chunk
+          const int j0 = 32 * half + 64 * c;         // first Q column of the chunk
           const uint32_t pcol = 32 * half + 16 * c;  // its packed P / dS column
-          uint32_t s[32], dp[32];
-          tmem_ld32x2(tl + C::cS + j0, tl + C::cDP + j0, s, dp);
-          uint32_t pk[16], dk[16];
+          uint32_t s[32];
+          tmem_ld32(tl + C::cS + j0, s);
+          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int qi = j0 + e + u;
-              float pr = ex2(fmaf(__uint_as_float(s[e + u]), p.scale_log2, -sL[qi]));
-              if (!row_ok || (p.causal && qbase + qi < kv_g)) pr = 0.f;
-              pv[u] = pr;
-              dv[u] = pr * (__uint_as_float(dp[e + u]) - sDl[qi]);
-            }
-            pk[e >> 1] = pack_bf16(pv[0], pv[1]);
-            dk[e >> 1] = pack_bf16(dv[0], dv[1]);
+          for (int e = 0; e < 32; ++e) {
+            const int qi = j0 + e;
+            float pr = ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -sL[qi]));
+            if (!row_ok || (p.causal && qbase + qi < kv_g)) pr = 0.f;
+            pv[c][e] = pr;
           }
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16(pv[c][e], pv[c][e + 1]);
           tmem_st16(tl + C::cS + pcol, pk);
-          tmem_st16(tl + C::cDP + pcol, dk);
-          // dS into shared memory as the MN-major A operand of dQ = dS K: [q/64][kv][64 q]
+        }
+        tmem_st_wait();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[bPFull]);
+      mbar_wait(&bars[bDpFull], sf_phase, g);
+      sf_phase ^= 1;
+      if (!warp_aborted(g)) {
+        tc_fence_after();
+        // pass B: dS = P * (dP - delta), packed bf16 into the dP^T columns and into
+        // shared memory as the MN-major A operand of dQ = dS K: [q/64][kv][64 q]
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          const int j0 = 32 * half + 64 * c;
+          const uint32_t pcol = 32 * half + 16 * c;
           uint8_t *rowp = sDS + (j0 >> 6) * C::kDsPanel + L * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int chunk = ((j0 & 63) >> 3) + i;
-            *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (L & 7)) << 4)) =
-                make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+          for (int sb = 0; sb < 2; ++sb) {  // 16 columns at a time keeps register use down
+            uint32_t dp[16];
+            tmem_ld16(tl + C::cDP + j0 + 16 * sb, dp);
+            uint32_t dk[8];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const int qi = j0 + 16 * sb + e;
+              const float d0 = pv[c][16 * sb + e] * (__uint_as_float(dp[e]) - sDl[qi]);
+              const float d1 = pv[c][16 * sb + e + 1] * (__uint_as_float(dp[e + 1]) - sDl[qi + 1]);
+              dk[e >> 1] = pack_bf16(d0, d1);
+            }
+            tmem_st8(tl + C::cDP + pcol + 8 * sb, dk);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              const int chunk = ((j0 & 63) >> 3) + 2 * sb + i;
+              *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (L & 7)) << 4)) =
+                  make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+            }
           }
         }
         tmem_st_wait();
@@ -379,66 +495,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[bPdsFull]);
+        mbar_arrive(&bars[bDsFull]);
         mbar_arrive(&qempty[st]);  // this warp is done with the stage's LSE / delta
       }
       st = (st + 1 == C::kStages) ? 0 : st + 1;
     }
   } else {
     // ------------------------------------------------------------ reduction + epilogue
-    regs_inc();
+    regs_reduce();
     const int sub = warp & 3;
     const int L = sub * 32 + lane;            // Q row of dQ, KV row of dK/dV
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    const bool ordered = p.ordered != 0;
-    const bool leader = threadIdx.x == kRedWarp0 * 32;
+    constexpr int kHalfChunks = D / 8;        // 16-byte chunks per half of a dQ row
     uint32_t dq_phase = 0, dkvf_phase = 0;
+    int st = 0;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
     for (int t = t_begin; t < t_end; ++t) {
       const int4 tk = nxt;
       if (t + 1 < t_end) nxt = tasks[t + 1];
-      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
+      const int bh = tk.x, kv = tk.y;
       const bool last = tk.w & kTaskLastFlag;
-      // -------- dQ partial: TMEM -> registers, then the ordered reduction
+      // -------- dQ partial: TMEM -> shared memory in the accumulator's tile layout
+      // [D/4][T][4]; chunks of the first half go to the Q buffer, the rest to dO's.
+      uint8_t *stage0 = smem + C::oQ + st * C::kQBytes;
+      uint8_t *stage1 = smem + C::oDO + st * C::kQBytes;
       mbar_wait(&bars[bDqFull], dq_phase, g);
       dq_phase ^= 1;
-      float acc[D];
       if (!warp_aborted(g)) {
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(tl + C::cDQ(c0 >> 6) + (c0 & 63), r);
+          tmem_ld32(tl + C::cDQ + c0, r);
+          if (L < T) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[c0 + e] = __uint_as_float(r[e]);
-        }
-        tc_fence_before();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[bTmemFree]);
-      int *sem = p.sem + (size_t)bh * p.n + q;
-      if (ordered) {
-        if (leader && !*g.abort) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(sem) != rank) {
-            if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
-              guard_fail(g, kStatusSemTimeout);
-              break;
+            for (int i = 0; i < 8; ++i) {
+              const int c = c0 / 4 + i;
+              uint8_t *buf = (c < kHalfChunks) ? stage0 : stage1;
+              const int cc = (c < kHalfChunks) ? c : c - kHalfChunks;
+              *reinterpret_cast<uint4 *>(buf + ((size_t)cc * T + L) * 16) =
+                  make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
             }
           }
         }
-        named_bar(kRedBar, kRedThreads);
+        tc_fence_before();
       }
-      if (!*g.abort && L < T) {
-        float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
-#pragma unroll
-        for (int c = 0; c < D / 4; ++c)
-          red_add_v4(dst + ((size_t)c * T + L) * 4, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
-      }
-      if (ordered) {
-        __threadfence();
-        named_bar(kRedBar, kRedThreads);
-        if (leader && !*g.abort) st_release_gpu(sem, rank + 1);
+      fence_proxy_async_smem();  // the staged tile is read next by the TMA engine
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[bTmemFree]);
+        mbar_arrive(&staged[st]);
       }
       // -------- end of a KV run: dK, dV out of TMEM
       if (last) {
@@ -477,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[bDkvEmpty]);
       }
+      st = (st + 1 == C::kStages) ? 0 : st + 1;
     }
   }
 
