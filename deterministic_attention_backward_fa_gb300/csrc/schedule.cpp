@@ -267,11 +267,15 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
   if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1) return -1;
   const long long nch = (long long)BH * chains_per_head(mode, n);
   const int gang = chains_per_head(mode, n);
+  // The cyclic schedules (shift, symmetric shift) make every chain of a head
+  // wait on its neighbour in the gang, so a gang split over time stalls; they
+  // only take whole gangs (the pages' setting: one SM per chain of a gang).
+  const bool cyclic = (mode == kShift || mode == kSymmetricShift);
   std::vector<int> cand;
   const int top = (int)std::min<long long>(P_max, nch);
-  cand.push_back(top);
+  if (!cyclic) cand.push_back(top);
   for (int m = (top / gang) * gang; m >= gang && (int)cand.size() < 16; m -= gang)
-    if (m != top) cand.push_back(m);
+    if (cyclic || m != top) cand.push_back(m);
   const HeadPlan hp = head_plan(mode, n, causal);
   const std::vector<int> hpred = head_pred(hp, n);
   int best = -1;

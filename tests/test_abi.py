@@ -79,7 +79,9 @@ def test_cta_choice_is_best_simulated(BH, n, causal, mode):
     chosen = dash.dash_choose_ctas(BH, n, causal, mode, P_max)
     gang = n // 2 if mode == "symmetric_shift" else n
     top = min(P_max, BH * gang)
-    cands = [top] + [m for m in range((top // gang) * gang, gang - 1, -gang) if m != top][:15]
+    cyclic = mode in ("shift", "symmetric_shift")
+    mults = [m for m in range((top // gang) * gang, gang - 1, -gang)]
+    cands = mults[:16] if cyclic else ([top] + [m for m in mults if m != top][:15])
     spans = {}
     for P in cands:
         try:
