@@ -13,23 +13,26 @@
 //   3. dash_bwd_convert: dQ = bf16(scale * accumulator).
 //
 // Main-kernel roles (512 threads, four warpgroups):
-//   warp 0       TMA producer (K/V once per KV run, Q/dO/LSE/delta per task)
+//   warp 0       TMA producer: K/V once per KV run, Q and LSE per task
+//   warp 2       TMA producer: dO and delta per task (a separate ring, so a
+//                Q tile can land while the dO buffer still stages dQ)
 //   warp 1       tensor-memory owner and single-lane tcgen05 MMA issuer
+//   warp 3       idle (gives its registers to the other warpgroups)
 //   warps 4-11   softmax: warp w handles TMEM sub-partition w % 4 (32 KV rows)
-//                and half of the Q columns of S^T / dP^T; recomputes P,
-//                forms dS and writes both back as bf16
-//   warps 2, 3   reduce issuers, taking tasks alternately: wait until the
-//                task's dQ partial is staged, acquire the dQ tile's semaphore
-//                at the task's rank, have the TMA engine add the staged tile
-//                into the fp32 accumulator (bulk reduce-add; rank 0 of an
-//                ordered schedule stores instead, so the accumulator needs no
-//                zeroing), hand the stage back to the producer once the TMA
-//                has read it, and release rank + 1 once the add has completed
-//   warps 12-15  reduction: drain the dQ partial from TMEM into shared memory
-//                (the task's own Q + dO stage, which the MMAs no longer read
-//                and which has exactly the size of the fp32 dQ tile); at the
-//                end of a KV run, write dK and dV
-// setmaxnreg gives the softmax warpgroups more registers than the others.
+//                and half of the Q columns.  Pass A turns S^T into P and
+//                stores it back packed as bf16 in tensor memory; pass B forms
+//                dS = P (dP - delta) and writes it to shared memory
+//   warps 12-15  dQ reduction: move the task's dQ partial from TMEM into
+//                registers (tensor memory is free again at once), acquire the
+//                dQ tile's semaphore at the task's rank, stage the partial in
+//                the task's dO buffer (half 1) and Q buffer (half 0, once dK
+//                has read Q), have the TMA engine add each half into the fp32
+//                accumulator (bulk reduce-add; rank 0 of an ordered schedule
+//                stores instead, so the accumulator needs no zeroing), hand
+//                the buffers back to the producers once the TMA has read them,
+//                and release rank + 1 once the adds have completed.  At the
+//                end of a KV run they write dK and dV
+// setmaxnreg gives the reduction warpgroup enough registers to hold a dQ row.
 //
 // All MMAs are M = 128: the lanes are KV rows for S^T = K Q^T, dP^T = V dO^T,
 // dV += P^T dO and dK += dS^T Q, and Q rows for dQ = dS K.  With 64-row tiles
@@ -37,17 +40,18 @@
 // and the Q side of dQ has 64 valid rows.
 //
 // Tensor memory (512 columns): S^T at 0, dP^T at 128, dV at 256, dK at 256+D.
-// A softmax warp of half h turns its columns [32h + 64c, +32) of S^T and dP^T
-// into packed bf16 P and dS at columns [32h + 16c, +16) of the same regions,
-// i.e. inside columns it has itself already read, so the two halves never
-// race.  P and dS then fill columns 0-63 of their regions.  dQ (one N = D
-// MMA) goes to the dP^T region when D = 128 (after dK has read dS there;
-// tcgen05 MMAs of one CTA run in issue order) and to columns 384+ when D = 64.
+// A softmax warp of half h turns its columns [32h + 64c, +32) of S^T into
+// packed bf16 P at columns [32h + 16c, +16), inside columns it has itself
+// already read, so the two halves never race; dV reads P from there as its
+// TMEM A operand.  dS lives in shared memory as [q/64][kv][64 q], which is the
+// MN-major A operand of dQ and the K-major A operand of dK at once.  dQ (one
+// N = D MMA) goes to the dP^T columns when D = 128 and to columns 384+ when
+// D = 64.
 //
-// Per task the MMA warp issues S^T, then dP^T; the softmax warps turn S^T into
-// P as soon as S^T is done (pass A) so that dV can start while they form dS
-// from dP^T (pass B); then dK and dQ.  The next task's S^T can be issued right
-// after dQ, while the reduction warps drain dQ; only dP^T waits for that drain.
+// Per task the MMA warp issues S^T, dP^T (once the previous dQ has left the
+// dP^T columns), dV, then, if the next task stays on this KV tile and its Q
+// tile has landed, the next S^T, so that pass A of the next task overlaps
+// this task's dQ and dK; then dQ and dK.
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -63,12 +67,14 @@ constexpr int kThreads = 512;
 constexpr int kSoftWarp0 = 4;
 constexpr int kNumSoftWarps = 8;
 constexpr int kRedWarp0 = 12;
+constexpr int kRedThreads = 128;
+constexpr int kDrainBar = 2;          // named barrier of the dQ-reduction warps
 constexpr int kNumRedWarps = 4;
 constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
 constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
-constexpr int kRegsSoftmax = 144;     // warpgroups 1, 2 after setmaxnreg.inc
+constexpr int kRegsSoftmax = 128;     // warpgroups 1, 2 (unchanged)
 static_assert(kRegsProducer < kRegsLaunch, "warpgroup 0 must give registers up before the others take them");
-constexpr int kRegsReduce = 136;      // warpgroup 3 after setmaxnreg.inc
+constexpr int kRegsReduce = 200;      // warpgroup 3 after setmaxnreg.inc (holds a dQ row)
 static_assert(kRegsProducer * 128 + 2 * kRegsSoftmax * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
               "register split exceeds the CTA's allocation");
 
@@ -92,7 +98,7 @@ struct BwdCfg {
   static constexpr uint32_t oLSE = oDS + kDsBytes;
   static constexpr uint32_t oDELTA = oLSE + kStages * T * 4;
   static constexpr uint32_t oBAR = oDELTA + kStages * T * 4;
-  static constexpr int kNumBars = 11 + 3 * kStages;
+  static constexpr int kNumBars = 12 + 5 * kStages;
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = oMISC + 16;
   // tensor-memory columns
@@ -105,7 +111,8 @@ struct BwdCfg {
 
 // barrier indices
 enum {
-  bKvFull = 0, bKvEmpty, bSFull, bDpFull, bPFull, bDsFull, bDqFull, bTmemFree, bDkvFull, bDkvEmpty, bFinal, bQFull0
+  bKvFull = 0, bKvEmpty, bSFull, bDpFull, bPFull, bDsFull, bDqFull, bTmemFree, bKDone, bDkvFull, bDkvEmpty, bFinal,
+  bQFull0
 };
 
 // setmaxnreg towards N registers per thread: .inc may only raise and .dec only
@@ -135,9 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::oBAR);
-  uint64_t *qfull = bars + bQFull0;
-  uint64_t *qempty = bars + bQFull0 + C::kStages;
-  uint64_t *staged = bars + bQFull0 + 2 * C::kStages;  // dQ partial of the stage's task is in smem
+  uint64_t *qfullQ = bars + bQFull0;                   // Q tile + LSE landed
+  uint64_t *qfullDO = bars + bQFull0 + C::kStages;      // dO tile + delta landed
+  uint64_t *qemptyQ = bars + bQFull0 + 2 * C::kStages;  // Q buffer + LSE free
+  uint64_t *qemptyDO = bars + bQFull0 + 3 * C::kStages; // dO buffer (+ staged dQ half) + delta free
+  // Q tile no longer read by the MMAs.  Per stage rather than per task: a
+  // stage is not reused before the drain warps release it, so they can never
+  // fall two phases behind on it (a per-task barrier that runs two phases
+  // ahead of its waiter is misread by the parity test).
+  uint64_t *qread = bars + bQFull0 + 4 * C::kStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
 
@@ -154,13 +167,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars[bDsFull], kNumSoftWarps);
     mbar_init(&bars[bDqFull], 1);
     mbar_init(&bars[bTmemFree], kNumRedWarps);
+    mbar_init(&bars[bKDone], 1);
     mbar_init(&bars[bDkvFull], 1);
     mbar_init(&bars[bDkvEmpty], kNumRedWarps);
     mbar_init(&bars[bFinal], 1);
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&qfull[s], 1);
-      mbar_init(&qempty[s], 1 + kNumSoftWarps);
-      mbar_init(&staged[s], kNumRedWarps);
+      mbar_init(&qfullQ[s], 1);
+      mbar_init(&qfullDO[s], 1);
+      mbar_init(&qemptyQ[s], 1 + kNumSoftWarps + 1);  // dK's commit, the softmax warps (LSE), the dQ half's TMA read
+      mbar_init(&qemptyDO[s], kNumSoftWarps + 1);   // the softmax warps (delta) + the dQ half's TMA read
+      mbar_init(&qread[s], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -186,12 +202,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     regs_dec();
-    if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------ producer
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // ------------------------------------------------------------ producers
+      // warp 0: K and V once per KV run, Q and LSE per task; warp 2: dO and
+      // delta per task.  Separate rings let Q arrive as soon as its buffer is
+      // free, independently of the dO buffer (which also stages half of dQ).
+      const bool qside = warp == 0;
+      uint64_t *full = qside ? qfullQ : qfullDO;
+      uint64_t *empty = qside ? qemptyQ : qemptyDO;
+      const CUtensorMap *map = qside ? &tmQ : &tmDO;
+      uint8_t *buf0 = smem + (qside ? C::oQ : C::oDO);
+      uint8_t *row0p = smem + (qside ? C::oLSE : C::oDELTA);
+      const float *rowsrc = qside ? p.lse2 : p.delta;
       uint32_t kv_e_phase = 0;
-      uint32_t qe_phase[C::kStages] = {};
-      uint32_t qf_last[C::kStages] = {};
-      bool q_used[C::kStages] = {};
+      uint32_t e_phase[C::kStages] = {};
+      uint32_t f_last[C::kStages] = {};
+      bool used[C::kStages] = {};
       bool kv_issued = false;
       uint32_t kv_last = 0, kv_fills = 0;
       int st = 0, runs = 0;
@@ -200,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 tk = nxt;
         if (t + 1 < t_end) nxt = tasks[t + 1];
         const int bh = tk.x, kv = tk.y, q = tk.z;
-        if (tk.w & kTaskFirstFlag) {
+        if (qside && (tk.w & kTaskFirstFlag)) {
           if (runs > 0) {
             mbar_wait(&bars[bKvEmpty], kv_e_phase, g);
             kv_e_phase ^= 1;
@@ -217,89 +243,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++kv_fills;
           }
         }
-        if (q_used[st]) {
-          mbar_wait(&qempty[st], qe_phase[st], g);
-          qe_phase[st] ^= 1;
+        if (used[st]) {
+          mbar_wait(&empty[st], e_phase[st], g);
+          e_phase[st] ^= 1;
         }
         if (!*g.abort) {
-          const uint32_t fill = q_used[st] ? (qf_last[st] ^ 1) : 0;
-          mbar_arrive_expect_tx(&qfull[st], 2 * C::kQBytes + 2 * T * 4);
-          for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_load_3d(smem + C::oQ + st * C::kQBytes + pn * C::kQPanel, &tmQ, &qfull[st], pn * 64, q * T, bh);
-            tma_load_3d(smem + C::oDO + st * C::kQBytes + pn * C::kQPanel, &tmDO, &qfull[st], pn * 64, q * T,
-                        bh);
-          }
-          const size_t row0 = ((size_t)bh * p.n + q) * T;
-          bulk_load(smem + C::oLSE + st * T * 4, p.lse2 + row0, T * 4, &qfull[st]);
-          bulk_load(smem + C::oDELTA + st * T * 4, p.delta + row0, T * 4, &qfull[st]);
-          qf_last[st] = fill;
-          q_used[st] = true;
+          const uint32_t fill = used[st] ? (f_last[st] ^ 1) : 0;
+          mbar_arrive_expect_tx(&full[st], C::kQBytes + T * 4);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(buf0 + st * C::kQBytes + pn * C::kQPanel, map, &full[st], pn * 64, q * T, bh);
+          bulk_load(row0p + st * T * 4, rowsrc + ((size_t)bh * p.n + q) * T, T * 4, &full[st]);
+          f_last[st] = fill;
+          used[st] = true;
         }
         st = (st + 1 == C::kStages) ? 0 : st + 1;
       }
       // let copies still in flight land before the CTA exits
       for (int s = 0; s < C::kStages; ++s)
-        if (q_used[s]) mbar_drain(&qfull[s], qf_last[s], g.limit_ns);
+        if (used[s]) mbar_drain(&full[s], f_last[s], g.limit_ns);
       if (kv_issued) mbar_drain(&bars[bKvFull], kv_last, g.limit_ns);
-    } else if ((warp == 2 || warp == 3) && lane == 0) {
-      // ------------------------------------------------------------ reduce issuers
-      const bool ordered = p.ordered != 0;
-      const int mine = warp - 2;
-      for (int t = t_begin + mine; t < t_end; t += 2) {
-        const int i = t - t_begin;
-        const int st = i % C::kStages;
-        const int4 tk = tasks[t];
-        const int bh = tk.x, q = tk.z, rank = tk.w & kTaskRankMask;
-        uint8_t *stage0 = smem + C::oQ + st * C::kQBytes;
-        uint8_t *stage1 = smem + C::oDO + st * C::kQBytes;
-        mbar_wait(&staged[st], (uint32_t)((i / C::kStages) & 1), g);
-        int *sem = p.sem + (size_t)bh * p.n + q;
-        if (ordered && !*g.abort) {
-          const uint64_t t0 = globaltimer_ns();
-          while (ld_acquire_gpu(sem) != rank) {
-            if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
-              guard_fail(g, kStatusSemTimeout);
-              break;
-            }
-          }
-        }
-        const bool go = !*g.abort;
-        if (go) {
-          float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
-          fence_proxy_async_global();
-          if (ordered && rank == 0) {  // first in the tile's order: store
-            bulk_store(dst, stage0, C::kQBytes);
-            bulk_store(dst + C::kQBytes / 4, stage1, C::kQBytes);
-          } else {
-            bulk_reduce_add_f32(dst, stage0, C::kQBytes);
-            bulk_reduce_add_f32(dst + C::kQBytes / 4, stage1, C::kQBytes);
-          }
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        mbar_arrive(&qempty[st]);  // the stage may be refilled
-        if (go) {
-          bulk_wait_all();  // the add has been performed in L2
-          if (ordered) {
-            fence_proxy_async_global();
-            st_release_gpu(sem, rank + 1);  // release: the next rank's acquire sees the sum
-          }
-        }
-      }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idS = idesc_bf16(128, T, 0, 0);    // S^T, dP^T: K-major A and B
-      constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A K-major (TMEM / smem), B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, D, 1, 1);    // dQ: MN-major A and B
       uint32_t kvf_phase = 0, dkve_phase = 0, pf_phase = 0, dsf_phase = 0, tf_phase = 0;
-      uint32_t qf_phase[C::kStages] = {};
+      uint32_t qfq_phase[C::kStages] = {}, qfd_phase[C::kStages] = {};
       int st = 0, runs = 0;
       const uint32_t sK = smem_u32(smem + C::oK), sV = smem_u32(smem + C::oV);
       const uint32_t sDS = smem_u32(smem + C::oDS);
       uint64_t dK_k = sw128_desc(sK, 16, 1024), dV_k = sw128_desc(sV, 16, 1024);  // K-major
       uint64_t dK_m = sw128_desc(sK, C::kKvPanel, 1024);                          // MN-major
-      uint64_t dDS_m = sw128_desc(sDS, C::kDsPanel, 1024);
-      bool issued = false;
+      uint64_t dDS_m = sw128_desc(sDS, C::kDsPanel, 1024);                        // dS as A of dQ
+      uint64_t dDS_k = sw128_desc(sDS, 16, 1024);                                 // dS^T as A of dK
+      bool issued = false, s_early = false;
+      // S^T = K Q^T into the S^T columns (M = 128 KV rows, N = T, K = D).  A
+      // descriptor plus (byte offset >> 4) addresses the same tile further on.
+      auto issue_s = [&](int stage) {
+        const uint64_t dQk = sw128_desc(smem_u32(smem + C::oQ + stage * C::kQBytes), 16, 1024);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
+          const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::cS, dK_k + off, dQk + offq, idS, kk > 0);
+        }
+        tc_commit(&bars[bSFull]);
+        issued = true;
+      };
       int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
       for (int t = t_begin; t < t_end; ++t) {
         const int4 tk = nxt;
@@ -314,27 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ++runs;
         }
-        mbar_wait(&qfull[st], qf_phase[st], g);
-        qf_phase[st] ^= 1;
         const uint32_t sQ = smem_u32(smem + C::oQ + st * C::kQBytes);
         const uint32_t sDO = smem_u32(smem + C::oDO + st * C::kQBytes);
         // keep the per-k-step descriptor sums inside the loop (hoisting all of
         // them out of it would need more registers than this warp has)
-        asm volatile("" : "+l"(dK_k), "+l"(dV_k), "+l"(dK_m), "+l"(dDS_m));
-        if (!*g.abort) {
-          tc_fence_after();
-          // S^T = K Q^T (M = 128 KV rows, N = T, K = D).  A descriptor plus
-          // (byte offset >> 4) addresses the same tile further on.
-          const uint64_t dQk = sw128_desc(sQ, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
-            const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::cS, dK_k + off, dQk + offq, idS, kk > 0);
-          }
-          tc_commit(&bars[bSFull]);
-          issued = true;
+        asm volatile("" : "+l"(dK_k), "+l"(dV_k), "+l"(dK_m), "+l"(dDS_m), "+l"(dDS_k));
+        if (!s_early) {  // S^T of this task was not issued during the previous one
+          mbar_wait(&qfullQ[st], qfq_phase[st], g);
+          qfq_phase[st] ^= 1;
+          if (!*g.abort) issue_s(st);
         }
+        mbar_wait(&qfullDO[st], qfd_phase[st], g);
+        qfd_phase[st] ^= 1;
         if (C::kDqInDp && t > t_begin) {  // the previous dQ sits in the dP^T columns
           mbar_wait(&bars[bTmemFree], tf_phase, g);
           tf_phase ^= 1;
@@ -370,6 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                        (!first || c + h + j > 0) ? 1u : 0u);
               }
         }
+        // The next task's S^T may go now (its columns are free once dV has read
+        // P; MMAs run in issue order) if it stays on this KV tile and its Q tile
+        // has already landed: the softmax warps then overlap it with dQ and dK.
+        s_early = false;
+        if (t + 1 < t_end && !(nxt.w & kTaskFirstFlag) && !*g.abort) {
+          const int st1 = (st + 1 == C::kStages) ? 0 : st + 1;
+          if (mbar_test(&qfullQ[st1], qfq_phase[st1])) {
+            qfq_phase[st1] ^= 1;
+            issue_s(st1);
+            s_early = true;
+          }
+        }
         mbar_wait(&bars[bDsFull], dsf_phase, g);
         dsf_phase ^= 1;
         if (!C::kDqInDp && t > t_begin) {
@@ -378,22 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!*g.abort) {
           tc_fence_after();
-          // dK += dS^T Q, same k-step order as dV
-#pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const uint32_t acol = 32 * h + 16 * c + 8 * j, q0 = 32 * h + 64 * c + 16 * j;
-                mma_ts(tmem + C::cDK, tmem + C::cDP + acol, dQm + ((q0 * 128) >> 4), idKV,
-                       (!first || c + h + j > 0) ? 1u : 0u);
-              }
-          // dQ = dS K (M = 128 Q rows, N = D, K = 128 KV rows)
+          // dQ = dS K first (it is on the critical path: the drain frees the
+          // next dP^T's columns), M = 128 Q rows, N = D, K = 128 KV rows
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ss(tmem + C::cDQ, dDS_m + ((kk * 2048) >> 4), dK_m + ((kk * 2048) >> 4), idQ, kk > 0);
           tc_commit(&bars[bDqFull]);
+          // dK += dS^T Q with dS^T read from shared memory as a K-major A operand
+          // ([q/64][kv][64 q] is exactly that layout), B = Q MN-major
+#pragma unroll
+          for (int kk = 0; kk < T / 16; ++kk) {
+            const uint32_t offa = ((kk >> 2) * C::kDsPanel + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::cDK, dDS_k + offa, dQm + ((kk * 16 * 128) >> 4), idKV,
+                   (!first || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&bars[bKDone]);   // the dS tile is no longer read
+          tc_commit(&qread[st]);      // nor is this task's Q tile
+          tc_commit(&qemptyQ[st]);
           if (last) {
             tc_commit(&bars[bDkvFull]);
             tc_commit(&bars[bKvEmpty]);
@@ -413,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kSoftWarp0) >> 2;
     const int L = sub * 32 + lane;            // this thread's KV row (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
-    uint32_t sf_phase = 0;
-    uint32_t qf_phase[C::kStages] = {};
+    uint32_t sf_phase = 0, dpf_phase = 0, kd_phase = 0;
+    uint32_t qfq_phase[C::kStages] = {}, qfd_phase[C::kStages] = {};
     int st = 0;
     uint8_t *sDS = smem + C::oDS;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
@@ -424,9 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kv = tk.y, q = tk.z;
       const float *sL = reinterpret_cast<const float *>(smem + C::oLSE + st * T * 4);
       const float *sDl = reinterpret_cast<const float *>(smem + C::oDELTA + st * T * 4);
-      mbar_wait(&qfull[st], qf_phase[st], g);
-      qf_phase[st] ^= 1;
+      mbar_wait(&qfullQ[st], qfq_phase[st], g);  // LSE
+      qfq_phase[st] ^= 1;
       mbar_wait(&bars[bSFull], sf_phase, g);
+      sf_phase ^= 1;
       float pv[C::kChunks][32];  // P of this thread's row and columns, kept for pass B
       if (!warp_aborted(g)) {
         tc_fence_after();
@@ -437,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;         // first Q column of the chunk
-          const uint32_t pcol = 32 * half + 16 * c;  // its packed P / dS column
+          const uint32_t pcol = 32 * half + 16 * c;  // its packed P column
           uint32_t s[32];
           tmem_ld32(tl + C::cS + j0, s);
           uint32_t pk[16];
@@ -456,17 +452,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[bPFull]);
-      mbar_wait(&bars[bDpFull], sf_phase, g);
-      sf_phase ^= 1;
+      if (lane == 0) {
+        mbar_arrive(&bars[bPFull]);
+        mbar_arrive(&qemptyQ[st]);  // this warp is done with the stage's LSE
+      }
+      mbar_wait(&qfullDO[st], qfd_phase[st], g);  // delta
+      qfd_phase[st] ^= 1;
+      mbar_wait(&bars[bDpFull], dpf_phase, g);
+      dpf_phase ^= 1;
+      if (t > t_begin) {  // the previous task's dQ and dK MMAs have read the dS tile
+        mbar_wait(&bars[bKDone], kd_phase, g);
+        kd_phase ^= 1;
+      }
       if (!warp_aborted(g)) {
         tc_fence_after();
-        // pass B: dS = P * (dP - delta), packed bf16 into the dP^T columns and into
-        // shared memory as the MN-major A operand of dQ = dS K: [q/64][kv][64 q]
+        // pass B: dS = P * (dP - delta), into shared memory as [q/64][kv][64 q]:
+        // the MN-major A operand of dQ = dS K and the K-major A operand of dK
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;
-          const uint32_t pcol = 32 * half + 16 * c;
           uint8_t *rowp = sDS + (j0 >> 6) * C::kDsPanel + L * 128;
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb) {  // 16 columns at a time keeps register use down
@@ -480,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float d1 = pv[c][16 * sb + e + 1] * (__uint_as_float(dp[e + 1]) - sDl[qi + 1]);
               dk[e >> 1] = pack_bf16(d0, d1);
             }
-            tmem_st8(tl + C::cDP + pcol + 8 * sb, dk);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
               const int chunk = ((j0 & 63) >> 3) + 2 * sb + i;
@@ -489,62 +492,113 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tmem_st_wait();
         fence_proxy_async_smem();
         tc_fence_before();
       }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bars[bDsFull]);
-        mbar_arrive(&qempty[st]);  // this warp is done with the stage's LSE / delta
+        mbar_arrive(&qemptyDO[st]);  // this warp is done with the stage's delta
       }
       st = (st + 1 == C::kStages) ? 0 : st + 1;
     }
   } else {
-    // ------------------------------------------------------------ reduction + epilogue
+    // ------------------------------------------------------------ dQ reduction + epilogue
     regs_reduce();
     const int sub = warp & 3;
     const int L = sub * 32 + lane;            // Q row of dQ, KV row of dK/dV
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
+    const bool ordered = p.ordered != 0;
+    const bool leader = threadIdx.x == kRedWarp0 * 32;
     constexpr int kHalfChunks = D / 8;        // 16-byte chunks per half of a dQ row
     uint32_t dq_phase = 0, dkvf_phase = 0;
+    uint32_t qr_phase[C::kStages] = {};
     int st = 0;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
     for (int t = t_begin; t < t_end; ++t) {
       const int4 tk = nxt;
       if (t + 1 < t_end) nxt = tasks[t + 1];
-      const int bh = tk.x, kv = tk.y;
+      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
       const bool last = tk.w & kTaskLastFlag;
-      // -------- dQ partial: TMEM -> shared memory in the accumulator's tile layout
-      // [D/4][T][4]; chunks of the first half go to the Q buffer, the rest to dO's.
-      uint8_t *stage0 = smem + C::oQ + st * C::kQBytes;
-      uint8_t *stage1 = smem + C::oDO + st * C::kQBytes;
+      // -------- dQ partial: TMEM -> registers; tensor memory is free at once.
       mbar_wait(&bars[bDqFull], dq_phase, g);
       dq_phase ^= 1;
-      if (!warp_aborted(g)) {
+      float acc[D];
+      const bool ok = !warp_aborted(g);
+      if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(tl + C::cDQ + c0, r);
-          if (L < T) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int c = c0 / 4 + i;
-              uint8_t *buf = (c < kHalfChunks) ? stage0 : stage1;
-              const int cc = (c < kHalfChunks) ? c : c - kHalfChunks;
-              *reinterpret_cast<uint4 *>(buf + ((size_t)cc * T + L) * 16) =
-                  make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
-            }
-          }
+          for (int e = 0; e < 32; ++e) acc[c0 + e] = __uint_as_float(r[e]);
         }
         tc_fence_before();
       }
-      fence_proxy_async_smem();  // the staged tile is read next by the TMA engine
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[bTmemFree]);
-        mbar_arrive(&staged[st]);
+      if (lane == 0) mbar_arrive(&bars[bTmemFree]);
+      // The tile's turn: acquire the semaphore while the partial waits in
+      // registers, so that no shared memory is held during the wait.
+      int *sem = p.sem + (size_t)bh * p.n + q;
+      float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
+      const bool first_rank = ordered && rank == 0;  // first in the tile's order: store
+      if (leader && ordered && !*g.abort) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(sem) != rank) {
+          if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+            guard_fail(g, kStatusSemTimeout);
+            break;
+          }
+        }
+      }
+      // The accumulator tile is [D/4][T][4] fp32; its second half goes through
+      // this task's dO buffer (free since dV has run) at once, its first half
+      // through the task's Q buffer once dK has read Q.  Each half is added by
+      // the TMA engine (bulk reduce-add, or a bulk store for rank 0); the two
+      // transfers overlap.
+      uint8_t *stageQ = smem + C::oQ + st * C::kQBytes;
+      uint8_t *stageDO = smem + C::oDO + st * C::kQBytes;
+#pragma unroll
+      for (int hf = 1; hf >= 0; --hf) {
+        uint8_t *stage = hf ? stageDO : stageQ;
+        if (hf == 0) {
+          mbar_wait(&qread[st], qr_phase[st], g);
+          qr_phase[st] ^= 1;
+        } else {
+          named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
+        }
+        if (ok && L < T) {
+#pragma unroll
+          for (int c = 0; c < kHalfChunks; ++c) {
+            const int a = 4 * (hf * kHalfChunks + c);
+            *reinterpret_cast<float4 *>(stage + ((size_t)c * T + L) * 16) =
+                make_float4(acc[a], acc[a + 1], acc[a + 2], acc[a + 3]);
+          }
+        }
+        fence_proxy_async_smem();  // the staged half is read next by the TMA engine
+        named_bar(kDrainBar, kRedThreads);
+        if (leader && !*g.abort) {
+          float *d = dst + (size_t)hf * (C::kQBytes / 4);
+          fence_proxy_async_global();
+          if (first_rank)
+            bulk_store(d, stage, C::kQBytes);
+          else
+            bulk_reduce_add_f32(d, stage, C::kQBytes);
+          bulk_commit();
+        }
+      }
+      if (leader) {
+        if (!*g.abort) bulk_wait_read_all();
+        mbar_arrive(&qemptyDO[st]);  // both buffers may be refilled
+        mbar_arrive(&qemptyQ[st]);
+        if (!*g.abort) {
+          bulk_wait_all();
+          if (ordered) {
+            fence_proxy_async_global();
+            st_release_gpu(sem, rank + 1);  // release: the next rank's acquire sees the sum
+          }
+        }
       }
       // -------- end of a KV run: dK, dV out of TMEM
       if (last) {
