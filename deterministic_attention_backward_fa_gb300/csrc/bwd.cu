@@ -429,6 +429,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kv_g = kv * T + L;
         const bool row_ok = (L < T) && (kv_g < p.S);
         const int qbase = q * T;
+        // Masking is needed only where a row lies past the sequence or, for a
+        // causal mask, the tile reaches above the diagonal; the test is made
+        // warp-uniform so that the unmasked path does not diverge.
+        const bool masked = __any_sync(0xffffffffu, !row_ok || (p.causal && qbase < kv_g));
         // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
@@ -437,12 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t s[32];
           tmem_ld32(tl + C::cS + j0, s);
           uint32_t pk[16];
+          if (masked) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int qi = j0 + e;
-            float pr = ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -sL[qi]));
-            if (!row_ok || (p.causal && qbase + qi < kv_g)) pr = 0.f;
-            pv[c][e] = pr;
+            for (int e = 0; e < 32; ++e) {
+              const int qi = j0 + e;
+              float pr = ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -sL[qi]));
+              if (!row_ok || (p.causal && qbase + qi < kv_g)) pr = 0.f;
+              pv[c][e] = pr;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              pv[c][e] = ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -sL[j0 + e]));
           }
 #pragma unroll
           for (int e = 0; e < 32; e += 2) pk[e >> 1] = pack_bf16(pv[c][e], pv[c][e + 1]);
