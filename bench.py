@@ -9,6 +9,9 @@ mask, half of it for a causal one) and the atomic schedule gives the ratio.
 
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
+--sweep times the pages' sweep instead (16384 tokens, S = 512 ... 16384, D = 64
+and 128, both masks) and prints one JSON line per configuration.
+
 --impl reference times the fp64 CPU oracle on the host cores instead (one head
 of the workload per step).  Under torchrun each rank runs an independent
 replica of the workload on its own GPU (there is no data exchange); rank 0
@@ -53,6 +56,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--schedules", default="", help="comma-separated subset of the workload's schedules")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the pages' sweep (16384 tokens, S = 512..16384, D = 64/128, both masks) "
+                         "and print one JSON line per configuration instead of the bench line")
     return ap.parse_args()
 
 
@@ -188,11 +194,60 @@ def run_reference(args, rank, world):
     return 0
 
 
+def run_sweep(args, dash):
+    """The pages' sweep, one GPU: every configuration and every schedule valid for its mask,
+    timed like the bench line (event-timed steps, L2 flushed between steps)."""
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    peaks, _ = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    for w in workloads.pages_sweep():
+        q, k, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
+        o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
+        dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+        res = {}
+        with ClockSampler(0) as clk:
+            for sched in w.schedules:
+                for _ in range(args.warmup):
+                    flush.fill_(1)
+                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile)
+                dash.dash_sync_status()
+                ms = []
+                for _ in range(args.steps):
+                    flush.fill_(1)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile)
+                    b.record(stream)
+                    b.synchronize()
+                    ms.append(a.elapsed_time(b))
+                dash.dash_sync_status()
+                res[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
+        det = {s: t for s, t in res.items() if s != "atomic"}
+        best = max(det, key=det.get)
+        print(json.dumps({"sweep": "pages_16k_tokens", "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
+                          "mask": "causal" if w.causal else "full", "tile": w.tile, "unit": "TFLOPS",
+                          "statistic": f"median of {args.steps} steps", "schedules": res,
+                          "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
+                          "ratio_vs_atomic": det[best] / res["atomic"], "clocks": clk.summary()}), flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.sweep:
+        import deterministic_attention_backward_fa_gb300 as dash
+        from deterministic_attention_backward_fa_gb300 import _build
+        torch.cuda.set_device(0)
+        if not _build.up_to_date():
+            _build.build()
+        dash.lib()
+        return run_sweep(args, dash)
 
     import deterministic_attention_backward_fa_gb300 as dash
     from deterministic_attention_backward_fa_gb300 import _build

@@ -30,7 +30,9 @@ the only library primitive used.
 Pins (tests/test_oracle.py): central finite differences of L = sum(O * dO),
 PyTorch's fp64 scaled-dot-product attention and its autograd on CPU,
 closed-form special cases (S = 1, q = 0, causal row 0), and invariants
-(rows of dS sum to zero, sum_j dK_j = 0, sum_j dV_j = sum_i dO_i).
+(rows of dS sum to zero, sum_j dK_j = 0, sum_j dV_j = sum_i dO_i).  The
+row-wise forms (``forward_rows``, ``backward_rows``), which check heads too
+long to form whole one row at a time, are pinned to PyTorch's autograd too.
 """
 from __future__ import annotations
 
@@ -131,3 +133,66 @@ def flops_fp64(B, H, S, D, causal: bool) -> float:
     matmuls per head, counted 2 flops per multiply-add; the causal case is
     counted at the full-matrix cost because the oracle forms whole matrices)."""
     return 10.0 * B * H * S * S * D
+
+
+def forward_rows(q, k, v, causal: bool, scale: float, rows):
+    """O and LSE of one head ([S, D] fp64 inputs) at the listed query rows only,
+    each row from the definition in the module docstring (O(S*D) per row, so it
+    serves heads too long to form whole).  Returns (O [len(rows), D], LSE [len(rows)])."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    S, D = q.shape
+    o = np.empty((len(rows), D))
+    lse = np.empty(len(rows))
+    for r, i in enumerate(rows):
+        s = scale * (k @ q[i])                      # s_ij over all keys j
+        if causal:
+            s[i + 1:] = -np.inf
+        m = s.max()
+        e = np.exp(s - m)
+        lse[r] = m + np.log(e.sum())
+        o[r] = (e / e.sum()) @ v
+    return o, lse
+
+
+def backward_rows(q, k, v, o, do, lse, causal: bool, scale: float, rows):
+    """dQ at the listed query rows and dK, dV at the listed key rows of one head.
+
+    Inputs are one head's [S, D] arrays and its LSE [S] (the O and LSE that the
+    backward is fed, like ``backward``).  Each row comes from the definition in
+    the module docstring, without forming an S x S matrix:
+      dQ_i = scale * sum_j P_ij (dP_ij - delta_i) k_j        (row i of P and dP)
+      dK_j = scale * sum_i P_ij (dP_ij - delta_i) q_i        (column j of P and dP)
+      dV_j = sum_i P_ij dO_i
+    Returns (dQ, dK, dV), each [len(rows), D] fp64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    o = np.asarray(o, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    lse = np.asarray(lse, dtype=np.float64)
+    S, D = q.shape
+    delta = (do * o).sum(axis=1)                    # delta_i for every query row
+    dq = np.empty((len(rows), D))
+    dk = np.empty((len(rows), D))
+    dv = np.empty((len(rows), D))
+    for r, i in enumerate(rows):
+        # query row i: P_i. and dP_i. over all keys
+        s = scale * (k @ q[i])
+        if causal:
+            s[i + 1:] = -np.inf
+        p = np.exp(s - lse[i])
+        dp = v @ do[i]
+        dq[r] = scale * ((p * (dp - delta[i])) @ k)
+        # key row j = i: P_.j and dP_.j over all queries
+        j = i
+        s = scale * (q @ k[j])
+        if causal:
+            s[:j] = -np.inf
+        p = np.exp(s - lse)
+        dp = do @ v[j]
+        dk[r] = scale * ((p * (dp - delta)) @ q)
+        dv[r] = p @ do
+    return dq, dk, dv

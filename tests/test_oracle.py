@@ -132,3 +132,26 @@ def test_head_subset_equals_full():
     for (b, h), g in sub.items():
         for x, y in zip(g, full):
             np.testing.assert_array_equal(x, y[b, h])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_oracle_matches_torch_autograd_and_full_backward(causal):
+    # the row-wise forms serve heads too long to form whole; pin them against
+    # PyTorch's fp64 attention and autograd, and against the whole-matrix oracle
+    S, D = 41, 16
+    scale = 0.35
+    q, k, v, do = (rnd((1, 1, S, D), 80 + i) for i in range(4))
+    rows = [0, 1, 20, 39, 40]
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    to.backward(torch.tensor(do, dtype=torch.float64))
+    o, lse = A.forward(q, k, v, causal, scale)
+    ro, rl = A.forward_rows(q[0, 0], k[0, 0], v[0, 0], causal, scale, rows)
+    np.testing.assert_allclose(ro, to.detach().numpy()[0, 0][rows], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(rl, lse[0, 0][rows], rtol=1e-13, atol=1e-13)
+    rq, rk, rv = A.backward_rows(q[0, 0], k[0, 0], v[0, 0], o[0, 0], do[0, 0], lse[0, 0], causal, scale, rows)
+    for got, grad in zip((rq, rk, rv), (tq.grad, tk.grad, tv.grad)):
+        np.testing.assert_allclose(got, grad.numpy()[0, 0][rows], rtol=1e-9, atol=1e-11)
+    full = A.backward(q, k, v, o, do, lse, causal, scale)
+    for got, f in zip((rq, rk, rv), full):
+        np.testing.assert_allclose(got, f[0, 0][rows], rtol=1e-12, atol=1e-13)

@@ -103,3 +103,23 @@ def make_inputs(B: int, H: int, S: int, D: int, gain: float = 1.0, seed: int = S
 
 def make_workload_inputs(w: Workload, seed: int = SEED):
     return make_inputs(w.B, w.H, w.S, w.D, w.gain, seed)
+
+
+# The pages' sweep (DASH paper write-up, experimental setup paragraph): the total
+# token count fixed at 16384, sequence lengths 512 to 16384 (batch = 16384 / S),
+# hidden size 2048 with head dimension 64 or 128 (so 32 or 16 heads), both masks.
+PAGES_SWEEP_TOKENS = 16384
+PAGES_SWEEP_HIDDEN = 2048
+PAGES_SWEEP_S = (512, 1024, 2048, 4096, 8192, 16384)
+
+
+def pages_sweep():
+    """The pages' sweep as workloads named ``sweep_{full|causal}_s{S}_d{D}``, tile 128."""
+    out = []
+    for causal in (False, True):
+        for D in (64, 128):
+            for S in PAGES_SWEEP_S:
+                B, H = PAGES_SWEEP_TOKENS // S, PAGES_SWEEP_HIDDEN // D
+                name = f"sweep_{'causal' if causal else 'full'}_s{S}_d{D}"
+                out.append(Workload(name, B, H, S, D, causal, 128, 1.0, _valid(causal, ALL_SCHEDULES)))
+    return out
