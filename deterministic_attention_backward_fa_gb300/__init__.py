@@ -60,6 +60,7 @@ _SIGS = {
     "dash_schedule_num_tasks": ([_I, _I, _I, _I], ctypes.c_longlong),
     "dash_build_schedule": ([_I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
+    "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_sync_status": ([_P], _I),
     "dash_release_workspace": ([], None),
     "dash_last_error": ([], ctypes.c_char_p),
@@ -204,6 +205,16 @@ def dash_build_schedule(BH: int, n: int, causal: bool, schedule, P: int, cost_c:
 
 def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
     return int(lib().dash_choose_ctas(BH, n, int(causal), _sched(schedule), max_ctas, cost_c, cost_r))
+
+
+def dash_choose_schedule(BH: int, n: int, causal: bool, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
+    """Host-only.  Returns (schedule name, CTA count, simulated makespan) of the
+    deterministic schedule with the smallest simulated makespan."""
+    P, ms = _I(0), ctypes.c_longlong(0)
+    s = lib().dash_choose_schedule(BH, n, int(causal), max_ctas, cost_c, cost_r, ctypes.byref(P), ctypes.byref(ms))
+    if s < 0:
+        raise DashError(1, dash_last_error())
+    return {v: k for k, v in SCHEDULES.items()}[s], P.value, ms.value
 
 
 def dash_sync_status(stream=None):

@@ -457,6 +457,20 @@ int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int ma
   return dash::choose_ctas(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r);
 }
 
+int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                         long long *makespan_out) {
+  int P = 0;
+  long long ms = 0;
+  const int s = dash::choose_schedule(BH, n, causal != 0, max_ctas, cost_c, cost_r, &P, &ms);
+  if (s < 0) {
+    dash::set_last_error("dash_choose_schedule: BH, n, max_ctas and the costs must be >= 1");
+    return -1;
+  }
+  if (ctas_out) *ctas_out = P;
+  if (makespan_out) *makespan_out = ms;
+  return s;
+}
+
 dash_status_t dash_sync_status(dash_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   cudaError_t e = cudaStreamSynchronize(stream);

@@ -39,4 +39,9 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
 // simulated makespan, ties to fewer CTAs.
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 
+// The deterministic schedule valid for the mask whose simulated makespan,
+// each at its own choose_ctas CTA count, is smallest (ties to the lower mode
+// number); fills its CTA count and makespan.  -1 on invalid arguments.
+int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out);
+
 }  // namespace dash

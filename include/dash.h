@@ -174,6 +174,19 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
 int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas,
                      int cost_c, int cost_r);
 
+/* Runtime schedule choice (DASH overview (zskr.cn), section 7: choosing the
+ * strategy from the run's own parameters; section 5.2 gives a static rule of
+ * thumb instead).  Among the deterministic schedules valid for the mask
+ * (serial, descending_q, and shift for a full mask or symmetric_shift for a
+ * causal one with n even), returns the one whose simulated makespan is
+ * smallest, each simulated at the CTA count dash_choose_ctas picks for it
+ * (at most max_ctas) with task costs C = cost_c and R = cost_r; ties go to the
+ * lower schedule number.  Writes that CTA count and makespan when the
+ * pointers are not NULL.  Returns -1 (and sets dash_last_error) when BH, n,
+ * max_ctas or a cost is below 1.  Host only. */
+int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                         long long *makespan_out);
+
 /* Synchronises `stream` and returns the device status of the calling
  * thread's current device workspace for that stream: DASH_OK, or
  * DASH_ERR_TIMEOUT if a bounded wait ran out since the last call (the word is

@@ -106,3 +106,27 @@ def test_error_codes_without_gpu():
     assert dash.dash_schedule_num_tasks(2, 8, True, "shift") == -1
     assert dash.dash_schedule_num_tasks(2, 8, True, "serial") == 2 * 36
     assert dash.dash_schedule_num_tasks(2, 7, True, "symmetric_shift") == -1
+
+
+@pytest.mark.parametrize("BH,n,causal,c,r", [(8, 4, False, 4, 1), (8, 4, False, 1, 4), (6, 8, True, 4, 1),
+                                             (6, 8, True, 1, 3), (4, 6, True, 4, 1), (3, 5, False, 2, 2),
+                                             (32, 16, True, 4, 1)])
+def test_schedule_choice_is_best_simulated(BH, n, causal, c, r):
+    # the runtime choice: smallest simulated makespan over the deterministic
+    # schedules valid for the mask, each at its chosen CTA count
+    P_max = 40
+    spans = {}
+    for mode in ("serial", "descending_q", "shift", "symmetric_shift"):
+        if (mode == "shift" and causal) or (mode == "symmetric_shift" and (not causal or n % 2)):
+            continue
+        P = dash.dash_choose_ctas(BH, n, causal, mode, P_max, c, r)
+        spans[mode] = (d.simulate(d.all_chains(mode, BH, n, causal), P, c, r).makespan, P)
+    best = min(s for s, _ in spans.values())
+    want = next(m for m in ("serial", "descending_q", "shift", "symmetric_shift") if m in spans and spans[m][0] == best)
+    assert dash.dash_choose_schedule(BH, n, causal, P_max, c, r) == (want, spans[want][1], best)
+
+
+def test_schedule_choice_rejects_bad_arguments():
+    with pytest.raises(dash.DashError):
+        dash.dash_choose_schedule(0, 4, False, 40)
+    assert "dash_choose_schedule" in dash.dash_last_error()
