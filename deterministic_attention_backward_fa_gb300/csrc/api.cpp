@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -96,10 +97,39 @@ struct DevBuf {
   }
 };
 
+// Copy streams and events of dash_attn_bwd_host, which pipelines the host
+// copies of one group of heads with the backward of another.
+constexpr int kHostChunks = 8;
+struct CopyLanes {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t landed[kHostChunks] = {}, done[kHostChunks] = {};
+  bool ready = false;
+  cudaError_t init() {
+    if (ready) return cudaSuccess;
+    cudaError_t e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking);
+    for (int c = 0; c < kHostChunks && e == cudaSuccess; ++c) {
+      e = cudaEventCreateWithFlags(&landed[c], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&done[c], cudaEventDisableTiming);
+    }
+    ready = (e == cudaSuccess);
+    return e;
+  }
+  ~CopyLanes() {
+    for (int c = 0; c < kHostChunks; ++c) {
+      if (landed[c]) cudaEventDestroy(landed[c]);
+      if (done[c]) cudaEventDestroy(done[c]);
+    }
+    if (in) cudaStreamDestroy(in);
+    if (out) cudaStreamDestroy(out);
+  }
+};
+
 struct Workspace {
   DevBuf accum, lse2, delta, sem, status;
   // device copies used by dash_attn_bwd_host
   DevBuf h_in[6], h_out[3];
+  CopyLanes lanes;
 };
 
 struct ScheduleEntry {
@@ -406,7 +436,8 @@ dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, co
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   const size_t tb = (size_t)B * H * S * D * 2, lb = (size_t)B * H * S * 4;
-  void *d[9];
+  uint8_t *d[9];
+  CopyLanes *lanes = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     Workspace *w = workspace(dev, stream);
@@ -416,20 +447,49 @@ dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, co
     for (int i = 0; i < 3; ++i)
       if ((e = w->h_out[i].reserve(tb)) != cudaSuccess)
         return fail(DASH_ERR_NO_MEMORY, "device output buffers: %s", cudaGetErrorString(e));
-    for (int i = 0; i < 6; ++i) d[i] = w->h_in[i].ptr;
-    for (int i = 0; i < 3; ++i) d[6 + i] = w->h_out[i].ptr;
+    for (int i = 0; i < 6; ++i) d[i] = static_cast<uint8_t *>(w->h_in[i].ptr);
+    for (int i = 0; i < 3; ++i) d[6 + i] = static_cast<uint8_t *>(w->h_out[i].ptr);
+    if ((e = w->lanes.init()) != cudaSuccess) return cuda_fail(e, "copy streams");
+    lanes = &w->lanes;
   }
-  const void *src[6] = {q, k, v, o, dout, lse};
-  for (int i = 0; i < 6; ++i)
-    if ((e = cudaMemcpyAsync(d[i], src[i], i == 5 ? lb : tb, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-      return cuda_fail(e, "cudaMemcpyAsync H2D");
-  st = bwd_impl(d[0], d[1], d[2], d[3], d[4], (const float *)d[5], d[6], d[7], d[8], B, H, S, D, causal, scale,
-                schedule, nullptr, stream);
-  if (st != DASH_OK) return st;
-  void *dst[3] = {dq, dk, dv};
-  for (int i = 0; i < 3; ++i)
-    if ((e = cudaMemcpyAsync(dst[i], d[6 + i], tb, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
-      return cuda_fail(e, "cudaMemcpyAsync D2H");
+  // Heads are independent problems and each head's dQ order depends on that
+  // head alone, so the heads are processed in up to kHostChunks groups: the
+  // inputs of one group travel to the device while the group before it runs,
+  // and its gradients travel back while the next one runs.  The results are
+  // those of one call over all heads, bit for bit.
+  const long long BH = (long long)B * H;
+  const int nch = BH >= 2 * kHostChunks ? kHostChunks : BH >= 8 ? 4 : BH >= 2 ? 2 : 1;
+  const long long per = (BH + nch - 1) / nch;
+  const uint8_t *src[6] = {static_cast<const uint8_t *>(q), static_cast<const uint8_t *>(k),
+                           static_cast<const uint8_t *>(v), static_cast<const uint8_t *>(o),
+                           static_cast<const uint8_t *>(dout), reinterpret_cast<const uint8_t *>(lse)};
+  uint8_t *dst[3] = {static_cast<uint8_t *>(dq), static_cast<uint8_t *>(dk), static_cast<uint8_t *>(dv)};
+  for (int c = 0; c < nch; ++c) {
+    const long long h0 = c * per, h1 = std::min(BH, h0 + per);
+    if (h0 >= h1) break;
+    const size_t t0 = (size_t)h0 * S * D * 2, tn = (size_t)(h1 - h0) * S * D * 2;
+    const size_t l0 = (size_t)h0 * S * 4, ln = (size_t)(h1 - h0) * S * 4;
+    for (int i = 0; i < 6; ++i)
+      if ((e = cudaMemcpyAsync(d[i] + (i == 5 ? l0 : t0), src[i] + (i == 5 ? l0 : t0), i == 5 ? ln : tn,
+                               cudaMemcpyHostToDevice, lanes->in)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync H2D");
+    if ((e = cudaEventRecord(lanes->landed[c], lanes->in)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, lanes->landed[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "copy-in ordering");
+    st = bwd_impl(d[0] + t0, d[1] + t0, d[2] + t0, d[3] + t0, d[4] + t0, reinterpret_cast<const float *>(d[5] + l0),
+                  d[6] + t0, d[7] + t0, d[8] + t0, 1, (int)(h1 - h0), S, D, causal, scale, schedule, nullptr, stream);
+    if (st != DASH_OK) {
+      cudaStreamSynchronize(lanes->in);
+      return st;
+    }
+    if ((e = cudaEventRecord(lanes->done[c], stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(lanes->out, lanes->done[c], 0)) != cudaSuccess)
+      return cuda_fail(e, "copy-out ordering");
+    for (int i = 0; i < 3; ++i)
+      if ((e = cudaMemcpyAsync(dst[i] + t0, d[6 + i] + t0, tn, cudaMemcpyDeviceToHost, lanes->out)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync D2H");
+  }
+  if ((e = cudaStreamSynchronize(lanes->out)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   return dash_sync_status(stream_);
 }

@@ -121,7 +121,12 @@ dash_status_t dash_attn_bwd_ex(const void *q, const void *k, const void *v, cons
 /* End-to-end backward from HOST buffers: copies the six inputs to the device,
  * runs dash_attn_bwd on `stream`, copies dq/dk/dv back and synchronises the
  * stream.  All pointers are host pointers (pinned memory gives full copy
- * bandwidth).  Device buffers are cached per (device, stream) and reused. */
+ * bandwidth).  The heads go in up to eight groups: each group's inputs are
+ * copied on an internal stream while the previous group's backward runs, and
+ * its gradients are copied back on another while the next one runs.  Heads
+ * are independent and each head's dQ order depends on that head alone, so the
+ * result equals a single dash_attn_bwd call over all heads, bit for bit.
+ * Device buffers and the copy streams are cached per (device, stream). */
 dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, const void *o,
                                  const void *dout, const float *lse,
                                  void *dq, void *dk, void *dv,

@@ -119,6 +119,27 @@ def test_host_buffer_entry_point_matches_device_path():
         assert torch.equal(a, b.cpu())
 
 
+@pytest.mark.parametrize("H", [5, 17])
+@pytest.mark.parametrize("sched", ["shift", "serial", "atomic"])
+def test_host_entry_point_in_head_groups_is_bit_identical(sched, H):
+    # ten heads go through the host entry point in four groups (3 + 3 + 3 + 1);
+    # thirty-four in groups of at most five (6 x 5 + 4)
+    # every head's dQ order is its own, so the bits equal one device call
+    # (atomic is compared within the tolerance: its order is not fixed)
+    P = Problem(2, H, 512, 128, False)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, False, P.scale)
+    ref = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, False, P.scale, sched)
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, ho, hdo, hl = (pin(t) for t in (P.q, P.k, P.v, o, P.do, lse))
+    outs = [torch.full_like(hq, float("nan")).pin_memory() for _ in range(3)]
+    dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, False, P.scale, sched)
+    for name, a, b in zip(("dQ", "dK", "dV"), outs, ref):
+        if sched == "atomic":
+            assert_close(f"host {name}", a.float(), b.double().cpu().numpy(), rel=1e-3, abs_=1e-2)
+        else:
+            assert torch.equal(a, b.cpu()), name
+
+
 def test_invalid_arguments_are_rejected():
     P = Problem(1, 2, 640, 64, True)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, True, P.scale)
