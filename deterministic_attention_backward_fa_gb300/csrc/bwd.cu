@@ -15,7 +15,7 @@
 // Main-kernel roles (512 threads, four warpgroups):
 //   warp 0       TMA producer: K/V once per KV run, Q and LSE per task
 //   warp 2       TMA producer: dO and delta per task (a separate ring, so a
-//                Q tile can land while the dO buffer still stages dQ)
+//                Q tile can land while the dO buffer is still busy)
 //   warp 1       tensor-memory owner and single-lane tcgen05 MMA issuer
 //   warp 3       idle (gives its registers to the other warpgroups)
 //   warps 4-11   softmax: warp w handles TMEM sub-partition w % 4 (32 KV rows)
@@ -23,15 +23,17 @@
 //                stores it back packed as bf16 in tensor memory; pass B forms
 //                dS = P (dP - delta) and writes it to shared memory
 //   warps 12-15  dQ reduction: move the task's dQ partial from TMEM into
-//                registers (tensor memory is free again at once), acquire the
-//                dQ tile's semaphore at the task's rank, stage the partial in
-//                the task's dO buffer (half 1) and Q buffer (half 0, once dK
-//                has read Q), have the TMA engine add each half into the fp32
-//                accumulator (bulk reduce-add; rank 0 of an ordered schedule
-//                stores instead, so the accumulator needs no zeroing), hand
-//                the buffers back to the producers once the TMA has read them,
-//                and release rank + 1 once the adds have completed.  At the
-//                end of a KV run they write dK and dV
+//                registers (tensor memory is free again at once); for an
+//                ordered schedule, acquire the dQ tile's semaphore at the
+//                task's rank, add the whole partial into the fp32 accumulator
+//                from registers with vector reductions (rank 0 stores instead,
+//                so the accumulator needs no zeroing) and release rank + 1
+//                once every reduction is issued and ordered before the
+//                release.  No shared memory is held while the chain advances.
+//                For the atomic schedule, half the partial is staged in the
+//                task's dO buffer (dV has read it) and added by the TMA engine
+//                (bulk reduce-add), the other half by vector reductions.  At
+//                the end of a KV run these warps write dK and dV
 // setmaxnreg gives the reduction warpgroup enough registers to hold a dQ row.
 //
 // All MMAs are M = 128: the lanes are KV rows for S^T = K Q^T, dP^T = V dO^T,
@@ -98,7 +100,7 @@ struct BwdCfg {
   static constexpr uint32_t oLSE = oDS + kDsBytes;
   static constexpr uint32_t oDELTA = oLSE + kStages * T * 4;
   static constexpr uint32_t oBAR = oDELTA + kStages * T * 4;
-  static constexpr int kNumBars = 12 + 5 * kStages;
+  static constexpr int kNumBars = 12 + 4 * kStages;
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = oMISC + 16;
   // tensor-memory columns
@@ -146,11 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *qfullDO = bars + bQFull0 + C::kStages;      // dO tile + delta landed
   uint64_t *qemptyQ = bars + bQFull0 + 2 * C::kStages;  // Q buffer + LSE free
   uint64_t *qemptyDO = bars + bQFull0 + 3 * C::kStages; // dO buffer (+ staged dQ half) + delta free
-  // Q tile no longer read by the MMAs.  Per stage rather than per task: a
-  // stage is not reused before the drain warps release it, so they can never
-  // fall two phases behind on it (a per-task barrier that runs two phases
-  // ahead of its waiter is misread by the parity test).
-  uint64_t *qread = bars + bQFull0 + 4 * C::kStages;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
 
@@ -174,9 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&qfullQ[s], 1);
       mbar_init(&qfullDO[s], 1);
-      mbar_init(&qemptyQ[s], 1 + kNumSoftWarps + 1);  // dK's commit, the softmax warps (LSE), the dQ half's TMA read
+      mbar_init(&qemptyQ[s], 1 + kNumSoftWarps);  // dK's commit + the softmax warps (LSE)
       mbar_init(&qemptyDO[s], kNumSoftWarps + 1);   // the softmax warps (delta) + the dQ half's TMA read
-      mbar_init(&qread[s], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -387,8 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (!first || kk > 0) ? 1u : 0u);
           }
           tc_commit(&bars[bKDone]);   // the dS tile is no longer read
-          tc_commit(&qread[st]);      // nor is this task's Q tile
-          tc_commit(&qemptyQ[st]);
+          tc_commit(&qemptyQ[st]);    // nor is this task's Q tile
           if (last) {
             tc_commit(&bars[bDkvFull]);
             tc_commit(&bars[bKvEmpty]);
@@ -522,7 +517,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = threadIdx.x == kRedWarp0 * 32;
     constexpr int kHalfChunks = D / 8;        // 16-byte chunks per half of a dQ row
     uint32_t dq_phase = 0, dkvf_phase = 0;
-    uint32_t qr_phase[C::kStages] = {};
     int st = 0;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
     for (int t = t_begin; t < t_end; ++t) {
@@ -562,52 +556,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      // The accumulator tile is [D/4][T][4] fp32; its second half goes through
-      // this task's dO buffer (free since dV has run) at once, its first half
-      // through the task's Q buffer once dK has read Q.  Each half is added by
-      // the TMA engine (bulk reduce-add, or a bulk store for rank 0); the two
-      // transfers overlap.
-      uint8_t *stageQ = smem + C::oQ + st * C::kQBytes;
-      uint8_t *stageDO = smem + C::oDO + st * C::kQBytes;
-#pragma unroll
-      for (int hf = 1; hf >= 0; --hf) {
-        uint8_t *stage = hf ? stageDO : stageQ;
-        if (hf == 0) {
-          mbar_wait(&qread[st], qr_phase[st], g);
-          qr_phase[st] ^= 1;
-        } else {
-          named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
-        }
+      // The accumulator tile is [D/4][T][4] fp32.  Ordered schedules add the
+      // whole partial from registers as vector reductions (stores for rank
+      // 0), so that no shared memory is held while the tile's chain advances
+      // and the next tasks' Q and dO tiles load at once.  The atomic schedule,
+      // whose adds never wait, stages the second half in this task's dO
+      // buffer (dV, its last reader, completed before dQ) for a bulk
+      // reduce-add by the TMA engine, which moves data faster than the
+      // vector reductions, and adds the first half from registers meanwhile.
+      named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
+      const int red_vecs = ordered ? 2 * kHalfChunks : kHalfChunks;
+      if (ordered) {
+        if (leader) mbar_arrive(&qemptyDO[st]);  // the dO buffer is not used for dQ
+      } else {
+        uint8_t *stage = smem + C::oDO + st * C::kQBytes;
         if (ok && L < T) {
 #pragma unroll
           for (int c = 0; c < kHalfChunks; ++c) {
-            const int a = 4 * (hf * kHalfChunks + c);
+            const int a = 4 * (kHalfChunks + c);
             *reinterpret_cast<float4 *>(stage + ((size_t)c * T + L) * 16) =
                 make_float4(acc[a], acc[a + 1], acc[a + 2], acc[a + 3]);
           }
         }
         fence_proxy_async_smem();  // the staged half is read next by the TMA engine
         named_bar(kDrainBar, kRedThreads);
-        if (leader && !*g.abort) {
-          float *d = dst + (size_t)hf * (C::kQBytes / 4);
-          fence_proxy_async_global();
-          if (first_rank)
-            bulk_store(d, stage, C::kQBytes);
-          else
-            bulk_reduce_add_f32(d, stage, C::kQBytes);
-          bulk_commit();
+        if (leader) {
+          if (!*g.abort) {
+            fence_proxy_async_global();
+            bulk_reduce_add_f32(dst + (size_t)(C::kQBytes / 4), stage, C::kQBytes);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&qemptyDO[st]);  // the dO buffer may be refilled
         }
       }
-      if (leader) {
-        if (!*g.abort) bulk_wait_read_all();
-        mbar_arrive(&qemptyDO[st]);  // both buffers may be refilled
-        mbar_arrive(&qemptyQ[st]);
-        if (!*g.abort) {
+      if (ok && L < T && !*g.abort) {
+        float *row = dst + (size_t)L * 4;
+        if (first_rank) {
+#pragma unroll
+          for (int c = 0; c < 2 * kHalfChunks; ++c)
+            *reinterpret_cast<float4 *>(row + (size_t)c * T * 4) =
+                make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 2 * kHalfChunks; ++c)
+            if (c < red_vecs)
+              red_add_v4(row + (size_t)c * T * 4, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+        }
+      }
+      if (ordered) {
+        named_bar(kDrainBar, kRedThreads);  // every thread's reductions are issued
+        if (leader && !*g.abort) {
           bulk_wait_all();
-          if (ordered) {
-            fence_proxy_async_global();
-            st_release_gpu(sem, rank + 1);  // release: the next rank's acquire sees the sum
-          }
+          fence_proxy_async_global();
+          st_release_gpu(sem, rank + 1);  // release: covers this CTA's adds of the tile
         }
       }
       // -------- end of a KV run: dK, dV out of TMEM

@@ -267,10 +267,12 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
   if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1) return -1;
   const long long nch = (long long)BH * chains_per_head(mode, n);
   const int gang = chains_per_head(mode, n);
-  // The cyclic schedules (shift, symmetric shift) make every chain of a head
-  // wait on its neighbour in the gang, so a gang split over time stalls; they
-  // only take whole gangs (the pages' setting: one SM per chain of a gang).
-  const bool cyclic = (mode == kShift || mode == kSymmetricShift);
+  // Shift makes every chain of a head wait on its neighbour in the gang, so a
+  // gang split over time stalls: it only takes whole gangs (the pages'
+  // setting, one SM per chain of a gang).  Symmetric shift also gets the
+  // full count to choose from: a split gang of it costs less than the idle
+  // SMs of whole gangs, in the simulation and on the GPU.
+  const bool cyclic = (mode == kShift);
   std::vector<int> cand;
   const int top = (int)std::min<long long>(P_max, nch);
   if (!cyclic) cand.push_back(top);

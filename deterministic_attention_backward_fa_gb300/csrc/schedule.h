@@ -35,8 +35,8 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
                            Schedule *out);
 
 // Candidate CTA counts (P_max and multiples of the gang size up to it, capped
-// at the number of chains; only the multiples for the cyclic schedules), best
-// simulated makespan, ties to fewer CTAs.
+// at the number of chains; only the multiples for shift), best simulated
+// makespan, ties to fewer CTAs.
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 
 // The deterministic schedule valid for the mask whose simulated makespan,

@@ -173,9 +173,9 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
 
 /* The CTA count the backward uses for a problem when num_ctas = 0: the
  * candidate (max_ctas, and the multiples of the schedule's gang size up to
- * it; only those multiples for shift and symmetric shift, whose chains wait on
- * their gang neighbours) whose simulated makespan is smallest, ties to fewer
- * CTAs.  Host only. */
+ * it; only those multiples for shift, whose chains wait on their gang
+ * neighbours so that a gang split over time stalls) whose simulated makespan
+ * is smallest, ties to fewer CTAs.  Host only. */
 int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas,
                      int cost_c, int cost_r);
 

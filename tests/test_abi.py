@@ -79,7 +79,7 @@ def test_cta_choice_is_best_simulated(BH, n, causal, mode):
     chosen = dash.dash_choose_ctas(BH, n, causal, mode, P_max)
     gang = n // 2 if mode == "symmetric_shift" else n
     top = min(P_max, BH * gang)
-    cyclic = mode in ("shift", "symmetric_shift")
+    cyclic = mode == "shift"   # only shift is restricted to whole gangs
     mults = [m for m in range((top // gang) * gang, gang - 1, -gang)]
     cands = mults[:16] if cyclic else ([top] + [m for m in mults if m != top][:15])
     spans = {}
