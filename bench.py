@@ -66,6 +66,20 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the job's time is its slowest rank's)."""
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, total_s: float) -> float:
+    """Throughput of the whole job: every rank runs its own replica of the workload."""
+    return world * flops_per_step * steps / total_s / 1e12
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -277,12 +291,6 @@ def main():
         if world > 1:
             torch.distributed.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
 
     gpu_index = local_rank
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -321,9 +329,9 @@ def main():
             launches += dash.KERNELS_PER_BWD * args.steps
             step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
             main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
-            total_s = max_over_ranks(sum(step_ms) / 1e3)
+            total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
             results[sched] = {"ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
-                              "tflops": world * flops * args.steps / total_s / 1e12}
+                              "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
     clocks = clk.summary()
 
     det = {s: r for s, r in results.items() if s != "atomic"} or results
@@ -343,7 +351,7 @@ def main():
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         dash.dash_attn_bwd_host(hq, hk, hv, ho, hdo, hl, *outs, w.causal, w.scale, best)
-    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, ho, hdo, hl))
     d2h = sum(t.numel() * t.element_size() for t in outs)
 
