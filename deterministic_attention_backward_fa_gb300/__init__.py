@@ -43,7 +43,8 @@ class BwdOptions(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int), ("num_ctas", ctypes.c_int), ("cost_c", ctypes.c_int),
                 ("cost_r", ctypes.c_int), ("spin_limit_ns", ctypes.c_longlong),
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
-                ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p)]
+                ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
+                ("dq_chains", ctypes.c_int)]
 
 
 _LIB = None
@@ -139,12 +140,13 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
-                     cta_off=None, main_events=None, stream=None):
+                     cta_off=None, main_events=None, stream=None, dq_chains=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
-    library records around the main kernel on the call's stream."""
+    library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
+    tile's ordered reduction into two chains by rank parity (see dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
-    opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None)
+    opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains)
     if main_events is not None:
         opt.main_begin_event = main_events[0].cuda_event
         opt.main_end_event = main_events[1].cuda_event

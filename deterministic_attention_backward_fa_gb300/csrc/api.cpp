@@ -235,6 +235,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const int c = (opt && opt->cost_c > 0) ? opt->cost_c : 4;
   const int r = (opt && opt->cost_r > 0) ? opt->cost_r : 1;
   const long long spin = (opt && opt->spin_limit_ns > 0) ? opt->spin_limit_ns : kDefaultSpinNs;
+  if (opt && (opt->dq_chains < 0 || opt->dq_chains > 2)) return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
+  const int chains = (mode != DASH_SCHED_ATOMIC && opt && opt->dq_chains == 2) ? 2 : 1;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -309,8 +311,9 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const long long rows_padded = (long long)n * T;
   const long long total_rows = (long long)BH * rows_padded;
   const long long accum_floats = total_rows * D;
-  if ((e = w->accum.reserve(accum_floats * 4)) != cudaSuccess || (e = w->lse2.reserve(total_rows * 4)) != cudaSuccess ||
-      (e = w->delta.reserve(total_rows * 4)) != cudaSuccess || (e = w->sem.reserve((size_t)BH * n * 4)) != cudaSuccess ||
+  if ((e = w->accum.reserve(accum_floats * chains * 4)) != cudaSuccess ||
+      (e = w->lse2.reserve(total_rows * 4)) != cudaSuccess || (e = w->delta.reserve(total_rows * 4)) != cudaSuccess ||
+      (e = w->sem.reserve((size_t)BH * n * chains * 4)) != cudaSuccess ||
       (e = ensure_status(w)) != cudaSuccess)
     return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
 
@@ -332,9 +335,17 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   // zeroing; the atomic schedule (and a caller-supplied table, which need not
   // hold every rank) adds into zeros.
   const bool ordered = mode != DASH_SCHED_ATOMIC;
-  pre.accum_floats = (ordered && !(opt && opt->tasks)) ? 0 : accum_floats;
+  // With two chains, chain 1 of a tile may receive nothing (a causal tile with
+  // one partial), so its accumulator starts at zero; chain 0 always holds rank 0.
+  float *accum = (float *)w->accum.ptr;
+  if (ordered && !(opt && opt->tasks)) {
+    pre.dq_accum = accum + accum_floats;
+    pre.accum_floats = chains > 1 ? accum_floats : 0;
+  } else {
+    pre.accum_floats = accum_floats * chains;
+  }
   pre.sem = (int *)w->sem.ptr;
-  pre.sem_count = BH * n;
+  pre.sem_count = BH * n * chains;
   pre.S = S;
   pre.D = D;
   pre.rows_padded = (int)rows_padded;
@@ -346,7 +357,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.cta_off = dev_off;
   mp.lse2 = pre.lse2;
   mp.delta = pre.delta;
-  mp.dq_accum = pre.dq_accum;
+  mp.dq_accum = accum;
   mp.sem = pre.sem;
   mp.dk = (__nv_bfloat16 *)dk;
   mp.dv = (__nv_bfloat16 *)dv;
@@ -358,13 +369,15 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.causal = causal ? 1 : 0;
   mp.ordered = mode != DASH_SCHED_ATOMIC;
   mp.spin_limit_ns = spin;
+  mp.chains = chains;
+  mp.chain_stride = accum_floats;
   if (opt && opt->main_begin_event && (e = cudaEventRecord((cudaEvent_t)opt->main_begin_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
   if ((e = dash::launch_bwd_main(D, T, maps, mp, P, stream)) != cudaSuccess) return cuda_fail(e, "main launch");
   if (opt && opt->main_end_event && (e = cudaEventRecord((cudaEvent_t)opt->main_end_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
-  if ((e = dash::launch_bwd_convert(D, T, pre.dq_accum, dq, opt ? opt->dq_accum_out : nullptr, scale, BH, S, n, sms,
-                                    stream)) != cudaSuccess)
+  if ((e = dash::launch_bwd_convert(D, T, accum, chains, accum_floats, dq, opt ? opt->dq_accum_out : nullptr,
+                                    scale, BH, S, n, sms, stream)) != cudaSuccess)
     return cuda_fail(e, "convert launch");
   return DASH_OK;
 }

@@ -543,13 +543,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[bTmemFree]);
       // The tile's turn: acquire the semaphore while the partial waits in
-      // registers, so that no shared memory is held during the wait.
-      int *sem = p.sem + (size_t)bh * p.n + q;
-      float *dst = p.dq_accum + ((size_t)bh * p.n + q) * (size_t)(T * D);
-      const bool first_rank = ordered && rank == 0;  // first in the tile's order: store
+      // registers, so that no shared memory is held during the wait.  With
+      // two chains, even ranks add into the first accumulator and odd ranks
+      // into the second, each in rank order behind its own semaphore.
+      const int chain = ordered ? rank % p.chains : 0, pos = ordered ? rank / p.chains : 0;
+      int *sem = p.sem + ((size_t)bh * p.n + q) * p.chains + chain;
+      float *dst = p.dq_accum + chain * p.chain_stride + ((size_t)bh * p.n + q) * (size_t)(T * D);
+      const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
       if (leader && ordered && !*g.abort) {
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(sem) != rank) {
+        while (ld_acquire_gpu(sem) != pos) {
           if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
             guard_fail(g, kStatusSemTimeout);
             break;
@@ -609,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader && !*g.abort) {
           bulk_wait_all();
           fence_proxy_async_global();
-          st_release_gpu(sem, rank + 1);  // release: covers this CTA's adds of the tile
+          st_release_gpu(sem, pos + 1);  // release: covers this CTA's adds of the tile
         }
       }
       // -------- end of a KV run: dK, dV out of TMEM
@@ -714,9 +717,12 @@ __global__ void __launch_bounds__(256) dash_bwd_preprocess(const __nv_bfloat16 *
   }
 }
 
-// dQ = bf16(scale * accumulator); optionally the unscaled fp32 accumulator in [BH][S][D].
+// dQ = bf16(scale * accumulator); optionally the unscaled fp32 accumulator in
+// [BH][S][D].  With two chains the accumulator is the sum of the two chains'
+// copies, chain 0 + chain 1, in that order.
 template <int D, int T>
-__global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict__ acc, __nv_bfloat16 *dq,
+__global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict__ acc, int chains,
+                                                       long long chain_stride, __nv_bfloat16 *dq,
                                                        float *acc_out, float scale, int S, int n,
                                                        long long total_vec4) {
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -729,8 +735,12 @@ __global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict_
     const long long bh = rowg / S;
     const int row = (int)(rowg - bh * S);
     const int qt = row / T, r = row - qt * T;
-    const float4 v =
-        *reinterpret_cast<const float4 *>(acc + (((size_t)bh * n + qt) * (size_t)(T * D)) + ((size_t)c * T + r) * 4);
+    const size_t at = (((size_t)bh * n + qt) * (size_t)(T * D)) + ((size_t)c * T + r) * 4;
+    float4 v = *reinterpret_cast<const float4 *>(acc + at);
+    if (chains > 1) {
+      const float4 w = *reinterpret_cast<const float4 *>(acc + chain_stride + at);
+      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+    }
     uint2 outv;
     outv.x = pack_bf16(scale * v.x, scale * v.y);
     outv.y = pack_bf16(scale * v.z, scale * v.w);
@@ -797,15 +807,19 @@ cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainPara
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_bwd_convert(int D, int T, const float *acc, void *dq, float *acc_out, float scale, int BH,
-                               int S, int n, int num_sms, cudaStream_t stream) {
+cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
+                               float *acc_out, float scale, int BH, int S, int n, int num_sms, cudaStream_t stream) {
   const long long total = (long long)BH * S * (D / 4);
   const int blocks = num_sms * 4;
   auto *out = (__nv_bfloat16 *)dq;
-  if (D == 64 && T == 64) dash_bwd_convert<64, 64><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
-  else if (D == 64 && T == 128) dash_bwd_convert<64, 128><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
-  else if (D == 128 && T == 64) dash_bwd_convert<128, 64><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
-  else dash_bwd_convert<128, 128><<<blocks, 256, 0, stream>>>(acc, out, acc_out, scale, S, n, total);
+  if (D == 64 && T == 64)
+    dash_bwd_convert<64, 64><<<blocks, 256, 0, stream>>>(acc, chains, chain_stride, out, acc_out, scale, S, n, total);
+  else if (D == 64 && T == 128)
+    dash_bwd_convert<64, 128><<<blocks, 256, 0, stream>>>(acc, chains, chain_stride, out, acc_out, scale, S, n, total);
+  else if (D == 128 && T == 64)
+    dash_bwd_convert<128, 64><<<blocks, 256, 0, stream>>>(acc, chains, chain_stride, out, acc_out, scale, S, n, total);
+  else
+    dash_bwd_convert<128, 128><<<blocks, 256, 0, stream>>>(acc, chains, chain_stride, out, acc_out, scale, S, n, total);
   return cudaGetLastError();
 }
 

@@ -33,8 +33,8 @@ struct BwdMainParams {
   const int *cta_off;    // gridDim.x + 1
   const float *lse2;     // [BH][n*T]  LSE * log2(e), +inf on padded rows
   const float *delta;    // [BH][n*T]  rowsum(dO * O), 0 on padded rows
-  float *dq_accum;       // [BH][n][D/4][T][4] fp32
-  int *sem;              // [BH][n]
+  float *dq_accum;       // [chains][BH][n][D/4][T][4] fp32
+  int *sem;              // [BH][n][chains]
   __nv_bfloat16 *dk;     // [BH][S][D]
   __nv_bfloat16 *dv;     // [BH][S][D]
   int *status;           // device status word
@@ -44,6 +44,8 @@ struct BwdMainParams {
   int causal;
   int ordered;           // 0: atomic (unordered) reduction
   long long spin_limit_ns;
+  int chains;            // ordered schedules: 1, or 2 (ranks split by parity, one accumulator each)
+  long long chain_stride;  // floats between the chains' accumulators
 };
 
 struct BwdPreParams {
@@ -72,7 +74,8 @@ size_t bwd_main_smem_bytes(int D, int T);
 cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
                             cudaStream_t stream);
-cudaError_t launch_bwd_convert(int D, int T, const float *acc, void *dq, float *acc_out, float scale, int BH,
+cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
+                               float *acc_out, float scale, int BH,
                                int S, int n, int num_sms, cudaStream_t stream);
 
 // Forward: Q/K/V maps with 128-row boxes.

@@ -208,9 +208,11 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   mp.causal = causal ? 1 : 0;
   mp.ordered = mode != DASH_SCHED_ATOMIC;
   mp.spin_limit_ns = 2000000000LL;
+  mp.chains = 1;
+  mp.chain_stride = 0;
   if ((e = dash::launch_bwd_main(D, T, maps, mp, sch.P, stream)) != cudaSuccess)
     return fail(DASH_ERR_CUDA, "main launch: %s", cudaGetErrorString(e));
-  if ((e = dash::launch_bwd_convert(D, T, pre.dq_accum, dq, nullptr, scale, (int)BH, S, n, sms, stream)) !=
+  if ((e = dash::launch_bwd_convert(D, T, pre.dq_accum, 1, 0, dq, nullptr, scale, (int)BH, S, n, sms, stream)) !=
       cudaSuccess)
     return fail(DASH_ERR_CUDA, "convert launch: %s", cudaGetErrorString(e));
 

@@ -105,6 +105,11 @@ typedef struct {
   const int32_t *cta_off;  /* with tasks: HOST array of num_ctas+1 offsets into tasks */
   void *main_begin_event;  /* optional cudaEvent_t recorded on `stream` just before the main kernel */
   void *main_end_event;    /* optional cudaEvent_t recorded on `stream` just after it (timing) */
+  int dq_chains;           /* ordered schedules: 0 or 1 = one chain per dQ tile, the pages' order; 2 = two
+                            * chains (an extension beyond the pages): the tile's even ranks add into one fp32
+                            * accumulator and its odd ranks into another, each in rank order behind its own
+                            * semaphore, and dQ = chain 0 + chain 1.  Deterministic, with a different
+                            * summation order from 1.  Ignored by the atomic schedule. */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is

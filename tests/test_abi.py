@@ -106,6 +106,11 @@ def test_error_codes_without_gpu():
     assert dash.dash_schedule_num_tasks(2, 8, True, "shift") == -1
     assert dash.dash_schedule_num_tasks(2, 8, True, "serial") == 2 * 36
     assert dash.dash_schedule_num_tasks(2, 7, True, "symmetric_shift") == -1
+    # dq_chains other than 0, 1, 2 is rejected before any CUDA call
+    fake = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced
+    opt = dash.BwdOptions(0, 0, 0, 0, 0, None, None, None, None, None, 3)
+    assert L.dash_attn_bwd_ex(*([fake] * 9), 1, 1, 128, 64, 0, 0.1, 1, ctypes.byref(opt), nul) == 1
+    assert "dq_chains" in dash.dash_last_error()
 
 
 @pytest.mark.parametrize("BH,n,causal,c,r", [(8, 4, False, 4, 1), (8, 4, False, 1, 4), (6, 8, True, 4, 1),

@@ -51,6 +51,32 @@ def test_bit_identical_across_runs(w):
     print(f"{w.name}: atomic bit-identical across {RUNS} runs: {atomic_identical}")
 
 
+@pytest.mark.parametrize("wname", ["full_s4096_d128", "causal_s16384_d128"])
+def test_two_dq_chains_bit_identical_across_runs(wname):
+    # the two-chain reduction is deterministic too: its order is fixed by rank parity
+    w = workloads.WORKLOADS[wname]
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    for sched in w.schedules:
+        if sched == "atomic":
+            continue
+        first = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, dq_accum=True, tile=w.tile,
+                              dq_chains=2)
+        outs = [torch.empty_like(x) for x in first]
+        same = True
+        for _ in range(RUNS - 1):
+            dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, outs[0], outs[1], outs[2], w.causal, P.scale,
+                                  sched, tile=w.tile, dq_accum_out=outs[3], dq_chains=2)
+            same = same and all(torch.equal(a, b) for a, b in zip(outs, first))
+        dash.dash_sync_status()
+        assert same, f"{wname}: {sched} with two dQ chains is not bit-identical across {RUNS} runs"
+        # dK and dV do not depend on the dQ order; dQ is within rounding of the one-chain order
+        one = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile)
+        assert torch.equal(one[1], first[1]) and torch.equal(one[2], first[2])
+        assert_close(f"{sched} two vs one chain dQ", first[0].float(), one[0].double().cpu().numpy(),
+                     rel=2e-3, abs_=1e-2)
+
+
 def test_deterministic_schedules_agree_within_tolerance():
     # different schedules reduce dQ in different orders: close, not equal bits
     w = workloads.WORKLOADS["causal_s2048_d128"]

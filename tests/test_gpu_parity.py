@@ -73,6 +73,23 @@ def test_forward_and_backward_match_oracle(B, H, S, D, causal, tile):
             assert_close(f"{sched} {name} (end to end)", x, r2)
 
 
+@pytest.mark.parametrize("B,H,S,D,causal,tile", [SMALL[2], SMALL[5], SMALL[6], SMALL[7]])
+def test_two_dq_chains_match_oracle(B, H, S, D, causal, tile):
+    # the two-chain reduction (even and odd ranks in separate accumulators)
+    # against the oracle, for every ordered schedule
+    P = Problem(B, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    q, k, v, do = P.f64
+    ref = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    for sched in schedules_for(causal, S, tile):
+        if sched == "atomic":
+            continue
+        got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, dq_chains=2)
+        dash.dash_sync_status()
+        for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert_close(f"{sched} two chains {name}", x, r)
+
+
 LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
 
 
