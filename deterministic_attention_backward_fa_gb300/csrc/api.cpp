@@ -140,7 +140,7 @@ struct ScheduleEntry {
 
 std::mutex g_mu;
 std::map<std::pair<int, void *>, std::unique_ptr<Workspace>> g_ws;
-std::map<std::tuple<int, int, int, int, int, int, int, int>, std::unique_ptr<ScheduleEntry>> g_sched;
+std::map<std::tuple<int, int, int, int, int, int, int, int, int>, std::unique_ptr<ScheduleEntry>> g_sched;
 std::map<int, int> g_sms;
 
 int sm_count(int dev) {
@@ -271,11 +271,16 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   } else {
     const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
     if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
-    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r);
+    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains);
     auto &ent = g_sched[key];
     if (!ent) {
       std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
-      const int Puse = want ? want : dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
+      // Shift takes whole gangs of CTAs because a gang split over time stalls
+      // on its single chain.  With two chains each tile's chain advances
+      // every other rank, a split gang no longer stalls, and all SMs pay.
+      int Puse = want;
+      if (!Puse && chains == 2 && mode == DASH_SCHED_SHIFT) Puse = (int)std::min<long long>(sms, (long long)BH * n);
+      if (!Puse) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
       if (Puse < 1) {
         g_sched.erase(key);
         return fail(DASH_ERR_UNSUPPORTED, "no CTA count up to %d SMs runs this schedule without deadlock", sms);

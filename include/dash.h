@@ -109,7 +109,8 @@ typedef struct {
                             * chains (an extension beyond the pages): the tile's even ranks add into one fp32
                             * accumulator and its odd ranks into another, each in rank order behind its own
                             * semaphore, and dQ = chain 0 + chain 1.  Deterministic, with a different
-                            * summation order from 1.  Ignored by the atomic schedule. */
+                            * summation order from 1.  With num_ctas = 0, shift then takes every SM
+                            * instead of whole gangs.  Ignored by the atomic schedule. */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
