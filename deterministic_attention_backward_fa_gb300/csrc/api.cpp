@@ -318,7 +318,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const long long accum_floats = total_rows * D;
   if ((e = w->accum.reserve(accum_floats * chains * 4)) != cudaSuccess ||
       (e = w->lse2.reserve(total_rows * 4)) != cudaSuccess || (e = w->delta.reserve(total_rows * 4)) != cudaSuccess ||
-      (e = w->sem.reserve((size_t)BH * n * chains * 4)) != cudaSuccess ||
+      (e = w->sem.reserve((size_t)BH * n * chains * dash::kSemStride * 4)) != cudaSuccess ||
       (e = ensure_status(w)) != cudaSuccess)
     return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
 
@@ -350,7 +350,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
     pre.accum_floats = accum_floats * chains;
   }
   pre.sem = (int *)w->sem.ptr;
-  pre.sem_count = BH * n * chains;
+  pre.sem_count = BH * n * chains * dash::kSemStride;
   pre.S = S;
   pre.D = D;
   pre.rows_padded = (int)rows_padded;

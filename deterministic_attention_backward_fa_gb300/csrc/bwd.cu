@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // two chains, even ranks add into the first accumulator and odd ranks
       // into the second, each in rank order behind its own semaphore.
       const int chain = ordered ? rank % p.chains : 0, pos = ordered ? rank / p.chains : 0;
-      int *sem = p.sem + ((size_t)bh * p.n + q) * p.chains + chain;
+      int *sem = p.sem + (((size_t)bh * p.n + q) * p.chains + chain) * kSemStride;
       float *dst = p.dq_accum + chain * p.chain_stride + ((size_t)bh * p.n + q) * (size_t)(T * D);
       const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
       if (leader && ordered && !*g.abort) {

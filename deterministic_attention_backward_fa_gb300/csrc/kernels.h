@@ -13,6 +13,10 @@ namespace dash {
 // Device status word values (first error wins).
 constexpr int kStatusMbarTimeout = 1;     // an mbarrier wait ran out
 constexpr int kStatusSemTimeout = 2;      // a dQ semaphore wait ran out
+// dQ semaphores sit one 32-byte L2 sector apart: neighbouring tiles' semaphores
+// are polled and released by different CTAs at the same time, and sharing a
+// sector serialises those accesses at the L2 slice.
+constexpr int kSemStride = 8;
 constexpr int kStatusSmemMisaligned = 3;  // dynamic shared memory not 1024-byte aligned
 
 // Dynamic shared memory requested by every kernel that allocates all 512
@@ -34,7 +38,7 @@ struct BwdMainParams {
   const float *lse2;     // [BH][n*T]  LSE * log2(e), +inf on padded rows
   const float *delta;    // [BH][n*T]  rowsum(dO * O), 0 on padded rows
   float *dq_accum;       // [chains][BH][n][D/4][T][4] fp32
-  int *sem;              // [BH][n][chains]
+  int *sem;              // [BH][n][chains], kSemStride ints apart
   __nv_bfloat16 *dk;     // [BH][S][D]
   __nv_bfloat16 *dv;     // [BH][S][D]
   int *status;           // device status word

@@ -118,7 +118,7 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   const size_t n_tasks = (size_t)dash::num_tasks((int)BH, n, causal != 0);
   size_t off = 0;
   const size_t o_status = off;  off += 256;
-  const size_t o_sem = off;     off += up256((size_t)BH * n * 4);
+  const size_t o_sem = off;     off += up256((size_t)BH * n * dash::kSemStride * 4);
   const size_t o_lse2 = off;    off += up256((size_t)rows * 4);
   const size_t o_delta = off;   off += up256((size_t)rows * 4);
   const size_t o_accum = off;   off += up256((size_t)rows * D * 4);
@@ -183,7 +183,7 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   pre.dq_accum = reinterpret_cast<float *>(base + o_accum);
   pre.accum_floats = rows * D;
   pre.sem = reinterpret_cast<int *>(base + o_sem);
-  pre.sem_count = (int)(BH * n);
+  pre.sem_count = (int)(BH * n * dash::kSemStride);
   pre.S = S;
   pre.D = D;
   pre.rows_padded = n * T;
