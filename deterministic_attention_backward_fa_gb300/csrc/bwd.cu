@@ -24,12 +24,14 @@
 //                dS = P (dP - delta) and writes it to shared memory
 //   warps 12-15  dQ reduction: move the task's dQ partial from TMEM into
 //                registers (tensor memory is free again at once); for an
-//                ordered schedule, acquire the dQ tile's semaphore at the
-//                task's rank, add the whole partial into the fp32 accumulator
-//                from registers with vector reductions (rank 0 stores instead,
-//                so the accumulator needs no zeroing) and release rank + 1
-//                once every reduction is issued and ordered before the
-//                release.  No shared memory is held while the chain advances.
+//                ordered schedule, acquire the dQ tile's semaphore (one 32-byte
+//                L2 sector each) at the task's rank, add the whole partial into
+//                the fp32 accumulator from registers with vector reductions
+//                (rank 0 stores instead, so the accumulator needs no zeroing)
+//                and release rank + 1 once every reduction is issued and
+//                ordered before the release.  No shared memory is held while
+//                the chain advances.  With two chains (an option) the tile's
+//                even and odd ranks go to two accumulators, each its own chain.
 //                For the atomic schedule, half the partial is staged in the
 //                task's dO buffer (dV has read it) and added by the TMA engine
 //                (bulk reduce-add), the other half by vector reductions.  At
@@ -560,9 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // The accumulator tile is [D/4][T][4] fp32.  Ordered schedules add the
-      // whole partial from registers as vector reductions (stores for rank
-      // 0), so that no shared memory is held while the tile's chain advances
-      // and the next tasks' Q and dO tiles load at once.  The atomic schedule,
+      // whole partial from registers as vector reductions (stores for the
+      // first rank of a chain), so that no shared memory is held while the
+      // tile's chain advances and the next tasks' Q and dO tiles load at once.  The atomic schedule,
       // whose adds never wait, stages the second half in this task's dO
       // buffer (dV, its last reader, completed before dQ) for a bulk
       // reduce-add by the TMA engine, which moves data faster than the
@@ -609,11 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ordered) {
         named_bar(kDrainBar, kRedThreads);  // every thread's reductions are issued
-        if (leader && !*g.abort) {
-          bulk_wait_all();
-          fence_proxy_async_global();
-          st_release_gpu(sem, pos + 1);  // release: covers this CTA's adds of the tile
-        }
+        // The release is cumulative: it covers the other threads' reductions,
+        // which the named barrier ordered before it.  Its fence waits until L2
+        // has them, so the next rank's adds land after these.
+        if (leader && !*g.abort) st_release_gpu(sem, pos + 1);
       }
       // -------- end of a KV run: dK, dV out of TMEM
       if (last) {
