@@ -655,6 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       st = (st + 1 == C::kStages) ? 0 : st + 1;
     }
+    if (leader && !ordered) bulk_wait_all();  // the atomic schedule's last bulk adds have landed
   }
 
   tc_fence_before();

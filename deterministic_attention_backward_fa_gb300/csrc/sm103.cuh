@@ -133,12 +133,6 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float *gdst, const void *ssr
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
-// Bulk (non-tensor) copy from shared into global memory, same alignment rules.
-__device__ __forceinline__ void bulk_store(float *gdst, const void *ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-               "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Shared-memory sources of every committed bulk group may be overwritten.
 __device__ __forceinline__ void bulk_wait_read_all() {
@@ -224,13 +218,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// Byte offset of element (row, col) in a 128B-swizzled tile stored as column
-// panels of 64 bf16: [col/64][row][128 B], 16-byte chunks XOR-ed with row % 8.
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col, uint32_t rows) {
-  const uint32_t panel = col >> 6, c = col & 63;
-  return panel * rows * 128u + row * 128u + ((((c >> 3) ^ (row & 7u)) << 4) | ((c & 7u) << 1));
-}
-
 // tcgen05.ld of 32 consecutive 32-bit columns for the warp's 32 lanes, waited on.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -282,13 +269,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
-// tcgen05.st of 8 consecutive 32-bit columns (not waited on: call tmem_st_wait()).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-
 // tcgen05.st of 16 consecutive 32-bit columns (not waited on: call tmem_st_wait()).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -313,7 +293,6 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
