@@ -679,42 +679,51 @@ __global__ void __launch_bounds__(256) dash_bwd_preprocess(const __nv_bfloat16 *
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   for (long long i = gtid; i < accum_vec4; i += nthreads) dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long long i = gtid; i < sem_count; i += nthreads) sem[i] = 0;
-  // one warp per padded row
+  // one warp per padded row, two rows per round so that two rows' loads are in
+  // flight at once (the kernel is bound by how many bytes each SM has in flight)
   const int lane = threadIdx.x & 31;
   const long long gwarp = gtid >> 5, nwarps = nthreads >> 5;
   constexpr int kPer = D / 32;  // elements per lane
-  for (long long row = gwarp; row < total_rows; row += nwarps) {
-    const long long bh = row / rows_padded;
-    const int r = (int)(row - bh * rows_padded);
-    float dl = 0.f, l2 = __int_as_float(0x7f800000);  // +inf: P = 0 for padded rows
-    if (r < S) {
-      const size_t base = ((size_t)bh * S + r) * D + lane * kPer;
-      float sum = 0.f;
-      if constexpr (kPer == 4) {
-        const uint2 a = *reinterpret_cast<const uint2 *>(o + base);
-        const uint2 b = *reinterpret_cast<const uint2 *>(dout + base);
-        const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-        const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+  constexpr int kRows = 2;
+  for (long long row0 = gwarp * kRows; row0 < total_rows; row0 += nwarps * kRows) {
+    float sum[kRows], l2[kRows];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
-          sum = fmaf(fa.x, fb.x, sum);
-          sum = fmaf(fa.y, fb.y, sum);
+    for (int j = 0; j < kRows; ++j) {
+      const long long row = row0 + j;
+      const long long bh = row / rows_padded;
+      const int r = (int)(row - bh * rows_padded);
+      sum[j] = 0.f;
+      l2[j] = __int_as_float(0x7f800000);  // +inf: P = 0 for padded rows
+      if (row < total_rows && r < S) {
+        const size_t base = ((size_t)bh * S + r) * D + lane * kPer;
+        if constexpr (kPer == 4) {
+          const uint2 a = *reinterpret_cast<const uint2 *>(o + base);
+          const uint2 b = *reinterpret_cast<const uint2 *>(dout + base);
+          const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+          const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+            sum[j] = fmaf(fa.x, fb.x, sum[j]);
+            sum[j] = fmaf(fa.y, fb.y, sum[j]);
+          }
+        } else {
+          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base);
+          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + base);
+          const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+          sum[j] = fmaf(fa.x, fb.x, fa.y * fb.y);
         }
-      } else {
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + base);
-        const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-        sum = fmaf(fa.x, fb.x, fa.y * fb.y);
+        l2[j] = lse[(size_t)bh * S + r] * 1.4426950408889634f;
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      dl = sum;
-      l2 = lse[(size_t)bh * S + r] * 1.4426950408889634f;
     }
-    if (lane == 0) {
-      delta[row] = dl;
-      lse2[row] = l2;
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], off);
+      if (lane == 0 && row0 + j < total_rows) {
+        delta[row0 + j] = sum[j];
+        lse2[row0 + j] = l2[j];
+      }
     }
   }
 }
@@ -730,8 +739,9 @@ __global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict_
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   constexpr int kChunks = D / 4;
+  // i enumerates (bh, row, chunk) with chunk fastest: output writes are contiguous
+#pragma unroll 2
   for (long long i = gtid; i < total_vec4; i += nthreads) {
-    // i enumerates (bh, row, chunk) with chunk fastest: output writes are contiguous
     const int c = (int)(i % kChunks);
     const long long rowg = i / kChunks;  // bh * S + row
     const long long bh = rowg / S;
@@ -788,7 +798,7 @@ size_t bwd_main_smem_bytes(int D, int T) {
 }
 
 cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream_t stream) {
-  const int blocks = num_sms * 4;
+  const int blocks = num_sms * 8;  // 2048 threads per SM
   if (a.D == 64)
     dash_bwd_preprocess<64><<<blocks, 256, 0, stream>>>(
         (const __nv_bfloat16 *)a.o, (const __nv_bfloat16 *)a.dout, a.lse, a.lse2, a.delta, (float4 *)a.dq_accum,
@@ -812,7 +822,7 @@ cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainPara
 cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
                                float *acc_out, float scale, int BH, int S, int n, int num_sms, cudaStream_t stream) {
   const long long total = (long long)BH * S * (D / 4);
-  const int blocks = num_sms * 4;
+  const int blocks = num_sms * 8;  // 2048 threads per SM
   auto *out = (__nv_bfloat16 *)dq;
   if (D == 64 && T == 64)
     dash_bwd_convert<64, 64><<<blocks, 256, 0, stream>>>(acc, chains, chain_stride, out, acc_out, scale, S, n, total);
