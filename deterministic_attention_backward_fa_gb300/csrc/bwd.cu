@@ -735,29 +735,47 @@ template <int D, int T>
 __global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict__ acc, int chains,
                                                        long long chain_stride, __nv_bfloat16 *dq,
                                                        float *acc_out, float scale, int S, int n,
-                                                       long long total_vec4) {
+                                                       long long total_rows) {
   const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
-  constexpr int kChunks = D / 4;
-  // i enumerates (bh, row, chunk) with chunk fastest: output writes are contiguous
-#pragma unroll 2
-  for (long long i = gtid; i < total_vec4; i += nthreads) {
-    const int c = (int)(i % kChunks);
-    const long long rowg = i / kChunks;  // bh * S + row
+  // Work item i = (group of 4 column chunks, row), rows fastest: a warp reads
+  // 32 consecutive rows of a chunk, which are contiguous in the accumulator's
+  // [D/4][T][4] tile layout, and each thread writes 32 contiguous bytes of dQ.
+  constexpr int kGroups = D / 16;
+  const long long total = total_rows * kGroups;
+  for (long long i = gtid; i < total; i += nthreads) {
+    const int g = (int)(i / total_rows);
+    const long long rowg = i - (long long)g * total_rows;  // bh * S + row
     const long long bh = rowg / S;
     const int row = (int)(rowg - bh * S);
     const int qt = row / T, r = row - qt * T;
-    const size_t at = (((size_t)bh * n + qt) * (size_t)(T * D)) + ((size_t)c * T + r) * 4;
-    float4 v = *reinterpret_cast<const float4 *>(acc + at);
-    if (chains > 1) {
-      const float4 w = *reinterpret_cast<const float4 *>(acc + chain_stride + at);
-      v = make_float4(v.x + w.x, v.y + w.y, v.z + w.z, v.w + w.w);
+    const size_t tile = ((size_t)bh * n + qt) * (size_t)(T * D);
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const size_t at = tile + ((size_t)(4 * g + k) * T + r) * 4;
+      v[k] = *reinterpret_cast<const float4 *>(acc + at);
+      if (chains > 1) {
+        const float4 w = *reinterpret_cast<const float4 *>(acc + chain_stride + at);
+        v[k] = make_float4(v[k].x + w.x, v[k].y + w.y, v[k].z + w.z, v[k].w + w.w);
+      }
     }
-    uint2 outv;
-    outv.x = pack_bf16(scale * v.x, scale * v.y);
-    outv.y = pack_bf16(scale * v.z, scale * v.w);
-    *reinterpret_cast<uint2 *>(dq + (size_t)rowg * D + c * 4) = outv;
-    if (acc_out) *reinterpret_cast<float4 *>(acc_out + (size_t)rowg * D + c * 4) = v;
+    uint4 o0, o1;
+    o0.x = pack_bf16(scale * v[0].x, scale * v[0].y);
+    o0.y = pack_bf16(scale * v[0].z, scale * v[0].w);
+    o0.z = pack_bf16(scale * v[1].x, scale * v[1].y);
+    o0.w = pack_bf16(scale * v[1].z, scale * v[1].w);
+    o1.x = pack_bf16(scale * v[2].x, scale * v[2].y);
+    o1.y = pack_bf16(scale * v[2].z, scale * v[2].w);
+    o1.z = pack_bf16(scale * v[3].x, scale * v[3].y);
+    o1.w = pack_bf16(scale * v[3].z, scale * v[3].w);
+    uint4 *out = reinterpret_cast<uint4 *>(dq + (size_t)rowg * D + 16 * g);
+    out[0] = o0;
+    out[1] = o1;
+    if (acc_out) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) *reinterpret_cast<float4 *>(acc_out + (size_t)rowg * D + 16 * g + 4 * k) = v[k];
+    }
   }
 }
 
@@ -821,7 +839,7 @@ cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainPara
 
 cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
                                float *acc_out, float scale, int BH, int S, int n, int num_sms, cudaStream_t stream) {
-  const long long total = (long long)BH * S * (D / 4);
+  const long long total = (long long)BH * S;  // rows
   const int blocks = num_sms * 8;  // 2048 threads per SM
   auto *out = (__nv_bfloat16 *)dq;
   if (D == 64 && T == 64)
