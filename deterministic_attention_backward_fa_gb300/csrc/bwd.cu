@@ -554,8 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
       if (leader && ordered && !*g.abort) {
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_gpu(sem) != pos) {
-          if (globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+        // the time limit is checked every 64 polls: a timer read per poll
+        // would stretch the gap between two polls
+        for (uint32_t it = 1; ld_acquire_gpu(sem) != pos; ++it) {
+          if ((it & 63) == 0 && globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
             guard_fail(g, kStatusSemTimeout);
             break;
           }
