@@ -26,7 +26,8 @@
 //                registers (tensor memory is free again at once); for an
 //                ordered schedule, acquire the dQ tile's semaphore (one 32-byte
 //                L2 sector each) at the task's rank, add the whole partial into
-//                the fp32 accumulator from registers with vector reductions
+//                the fp32 accumulator from registers with vector reductions,
+//                paced so that they do not clog the load/store queue
 //                (rank 0 stores instead, so the accumulator needs no zeroing)
 //                and release rank + 1 once every reduction is issued and
 //                ordered before the release.  No shared memory is held while
@@ -74,6 +75,10 @@ constexpr int kRedWarp0 = 12;
 constexpr int kRedThreads = 128;
 constexpr int kDrainBar = 2;          // named barrier of the dQ-reduction warps
 constexpr int kNumRedWarps = 4;
+// Pauses between the dQ reductions of a reduction warp (see the drain).  On
+// the ordered path they lie on the tile's chain, so they are short.
+constexpr unsigned kRedPauseOrderedNs = 16;  // after every reduction
+constexpr unsigned kRedPauseAtomicNs = 96;   // after every third reduction
 constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
 constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
 constexpr int kRegsSoftmax = 128;     // warpgroups 1, 2 (unchanged)
@@ -605,10 +610,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4 *>(row + (size_t)c * T * 4) =
                 make_float4(acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
         } else {
+          // The reductions are paced to about the rate at which the SM's path
+          // to L2 accepts them.  Issued in one burst they fill the load/store
+          // queue, and every shared-memory access of the other warps (mbarrier
+          // waits, the softmax's loads and stores of LSE, delta and dS) then
+          // waits behind them, which stalls the MMA pipeline.
 #pragma unroll
           for (int c = 0; c < 2 * kHalfChunks; ++c)
-            if (c < red_vecs)
+            if (c < red_vecs) {
               red_add_v4(row + (size_t)c * T * 4, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
+              if (c + 1 < red_vecs) {
+                if (ordered)
+                  __nanosleep(kRedPauseOrderedNs);
+                else if (c % 3 == 2)
+                  __nanosleep(kRedPauseAtomicNs);
+              }
+            }
         }
       }
       if (ordered) {
