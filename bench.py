@@ -8,7 +8,10 @@ deterministic schedule's TFLOPS (conventional count: 10*B*H*S^2*D for a full
 mask, half of it for a causal one) and the atomic schedule gives the ratio.
 The ordered schedules are timed a second time with the optional two-chain dQ
 reduction (dq_chains = 2, a different fixed summation order); those figures go
-to `extension_two_dq_chains` and never into `value`.
+to `extension_two_dq_chains` and never into `value`.  For a full mask, shift is
+also timed with fill (shift_fill = 1: the SMs that whole gangs of shift chains
+leave idle run some heads in the serial order), under `extension_shift_fill`,
+never in `value`.
 
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -61,6 +64,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-two-chains", action="store_true",
                     help="skip timing the optional two-chain dQ reduction (dq_chains = 2)")
+    ap.add_argument("--no-shift-fill", action="store_true",
+                    help="skip timing shift with fill (shift_fill = 1)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the pages' sweep (16384 tokens, S = 512..16384, D = 64/128, both masks) "
                          "and print one JSON line per configuration instead of the bench line")
@@ -307,11 +312,13 @@ def main():
 
     results = {}
     two_chains = {}   # the optional two-chain dQ reduction (an extension beyond the pages' order)
+    fill = {}         # shift with fill (an extension beyond the pages' schedules)
     launches = 0
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
-    runs = [(s, 1) for s in scheds] + [(s, 2) for s in scheds if s != "atomic" and not args.no_two_chains]
+    runs = [(s, 1, 0) for s in scheds] + [(s, 2, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
+    runs += [("shift", 1, 1)] if "shift" in scheds and not args.no_shift_fill else []
     with ClockSampler(gpu_index) as clk:
-        for sched, chains in runs:
+        for sched, chains, shift_fill in runs:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                     torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
@@ -321,7 +328,7 @@ def main():
             for _ in range(args.warmup):
                 flush.fill_(1)
                 dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                      dq_chains=chains)
+                                      dq_chains=chains, shift_fill=shift_fill)
             dash.dash_sync_status()
             barrier()
             torch.cuda.synchronize()
@@ -329,7 +336,8 @@ def main():
                 flush.fill_(1)   # evict the previous step's working set from L2
                 evs[i][0].record(stream)
                 dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                      main_events=(evs[i][1], evs[i][2]), dq_chains=chains)
+                                      main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
+                                      shift_fill=shift_fill)
                 evs[i][3].record(stream)
             torch.cuda.synchronize()
             barrier()
@@ -338,7 +346,7 @@ def main():
             step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
             main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
             total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-            (results if chains == 1 else two_chains)[sched] = {
+            (fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
                 "ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
                 "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
     clocks = clk.summary()
@@ -346,7 +354,7 @@ def main():
     det = {s: r for s, r in results.items() if s != "atomic"} or results
     best = max(det, key=lambda s: det[s]["tflops"])
     atomic = results.get("atomic")
-    for s, r in list(results.items()) + list(two_chains.items()):
+    for s, r in list(results.items()) + list(two_chains.items()) + list(fill.items()):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
 
     # end to end through the host-buffer entry point: H2D inputs, backward, D2H gradients
@@ -399,6 +407,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
             "extension_two_dq_chains": two_chains or None,
+            "extension_shift_fill": fill or None,
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -44,7 +44,7 @@ class BwdOptions(ctypes.Structure):
                 ("cost_r", ctypes.c_int), ("spin_limit_ns", ctypes.c_longlong),
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
-                ("dq_chains", ctypes.c_int)]
+                ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int)]
 
 
 _LIB = None
@@ -60,6 +60,8 @@ _SIGS = {
     "dash_attn_bwd_noalloc": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_schedule_num_tasks": ([_I, _I, _I, _I], ctypes.c_longlong),
     "dash_build_schedule": ([_I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
+    "dash_build_shift_fill": ([_I] * 5 + [_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                                          ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_sync_status": ([_P], _I),
@@ -140,13 +142,16 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
-                     cta_off=None, main_events=None, stream=None, dq_chains=0):
+                     cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
-    tile's ordered reduction into two chains by rank parity (see dash_bwd_options_t)."""
+    tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
+    shift backward with the serial schedule on the SMs that whole gangs leave idle (see
+    dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
-    opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains)
+    opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
+                     shift_fill)
     if main_events is not None:
         opt.main_begin_event = main_events[0].cuda_event
         opt.main_end_event = main_events[1].cuda_event
@@ -203,6 +208,20 @@ def dash_build_schedule(BH: int, n: int, causal: bool, schedule, P: int, cost_c:
                                      tasks.ctypes.data_as(ctypes.c_void_p), off.ctypes.data_as(ctypes.c_void_p),
                                      ctypes.byref(ms)))
     return tasks[:nt], off, int(ms.value)
+
+
+def dash_build_shift_fill(BH: int, n: int, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
+    """Host-only.  Returns (tasks int32 [N, 4], cta_off int32 [P+1], P, shift_heads, makespan)."""
+    nt = dash_schedule_num_tasks(BH, n, False, "shift")
+    if nt < 0:
+        raise DashError(2, "schedule invalid for this n")
+    tasks = np.zeros((max(nt, 1), 4), dtype=np.int32)
+    off = np.zeros(max_ctas + 1, dtype=np.int32)
+    P, hs, ms = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_longlong(0)
+    _check(lib().dash_build_shift_fill(BH, n, max_ctas, cost_c, cost_r, tasks.ctypes.data_as(ctypes.c_void_p),
+                                       off.ctypes.data_as(ctypes.c_void_p), ctypes.byref(P), ctypes.byref(hs),
+                                       ctypes.byref(ms)))
+    return tasks[:nt], off[:P.value + 1], int(P.value), int(hs.value), int(ms.value)
 
 
 def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):

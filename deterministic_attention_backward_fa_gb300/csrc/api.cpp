@@ -140,7 +140,7 @@ struct ScheduleEntry {
 
 std::mutex g_mu;
 std::map<std::pair<int, void *>, std::unique_ptr<Workspace>> g_ws;
-std::map<std::tuple<int, int, int, int, int, int, int, int, int>, std::unique_ptr<ScheduleEntry>> g_sched;
+std::map<std::tuple<int, int, int, int, int, int, int, int, int, int>, std::unique_ptr<ScheduleEntry>> g_sched;
 std::map<int, int> g_sms;
 
 int sm_count(int dev) {
@@ -237,6 +237,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const long long spin = (opt && opt->spin_limit_ns > 0) ? opt->spin_limit_ns : kDefaultSpinNs;
   if (opt && (opt->dq_chains < 0 || opt->dq_chains > 2)) return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
   const int chains = (mode != DASH_SCHED_ATOMIC && opt && opt->dq_chains == 2) ? 2 : 1;
+  if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1)) return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
+  const bool fill = mode == DASH_SCHED_SHIFT && chains == 1 && opt && opt->shift_fill == 1;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -271,22 +273,29 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   } else {
     const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
     if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
-    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains);
+    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains, fill ? 1 : 0);
     auto &ent = g_sched[key];
     if (!ent) {
       std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
       // Shift takes whole gangs of CTAs because a gang split over time stalls
       // on its single chain.  With two chains each tile's chain advances
       // every other rank, a split gang no longer stalls, and all SMs pay.
+      // With fill, the SMs that whole gangs leave idle run other heads in the
+      // serial order (num_ctas, if given, is the CTA budget).
       int Puse = want;
       if (!Puse && chains == 2 && mode == DASH_SCHED_SHIFT) Puse = (int)std::min<long long>(sms, (long long)BH * n);
-      if (!Puse) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
-      if (Puse < 1) {
+      if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
+      if (Puse < 1 && !fill) {
         g_sched.erase(key);
         return fail(DASH_ERR_UNSUPPORTED, "no CTA count up to %d SMs runs this schedule without deadlock", sms);
       }
       dash::Schedule sch;
-      why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch);
+      if (fill) {
+        why = dash::build_shift_fill(BH, n, want ? want : sms, c, r, &sch, nullptr);
+        Puse = sch.P;
+      } else {
+        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch);
+      }
       if (!why.empty()) {
         g_sched.erase(key);
         return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
@@ -527,6 +536,23 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
   if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
   std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
   std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
+  if (makespan_out) *makespan_out = s.makespan;
+  return DASH_OK;
+}
+
+dash_status_t dash_build_shift_fill(int BH, int n, int max_ctas, int cost_c, int cost_r, int32_t *tasks_out,
+                                    int32_t *cta_off_out, int *ctas_out, int *shift_heads_out, long long *makespan_out) {
+  if (!tasks_out || !cta_off_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
+  std::string why = dash::check_mode(dash::kShift, n, false);
+  if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  dash::Schedule s;
+  int hs = 0;
+  why = dash::build_shift_fill(BH, n, max_ctas, cost_c, cost_r, &s, &hs);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
+  std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
+  if (ctas_out) *ctas_out = s.P;
+  if (shift_heads_out) *shift_heads_out = hs;
   if (makespan_out) *makespan_out = s.makespan;
   return DASH_OK;
 }

@@ -293,6 +293,63 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
   return best;
 }
 
+std::string build_shift_fill(int BH, int n, int P_max, int c, int r, Schedule *out, int *shift_heads) {
+  std::string e = check_mode(kShift, n, false);
+  if (!e.empty()) return e;
+  if (BH < 1 || P_max < 1 || c < 1 || r < 1) return "BH, P and the costs must be >= 1";
+  const int per_wave = P_max / n;  // heads whose gangs fit side by side
+  const int G = per_wave * n, F = P_max - G;
+  if (per_wave == 0 || F == 0 || BH <= per_wave) {
+    const int P = choose_ctas(BH, n, false, kShift, P_max, c, r);
+    if (P < 1) return "no CTA count runs this schedule without deadlock";
+    if (shift_heads) *shift_heads = BH;
+    return build_schedule(BH, n, false, kShift, P, c, r, out);
+  }
+  const HeadPlan hs_plan = head_plan(kShift, n, false), se_plan = head_plan(kSerial, n, false);
+  const std::vector<int> hs_pred = head_pred(hs_plan, n), se_pred = head_pred(se_plan, n);
+  int best_hs = -1, best_P1 = 0, best_P2 = 0;
+  long long best_ms = 0;
+  const int waves = (BH + per_wave - 1) / per_wave;
+  for (int k = waves; k >= 1; --k) {  // more shift heads first, so that ties keep them
+    const int hs = std::min(BH, k * per_wave), rest = BH - hs;
+    const int P1 = (int)std::min<long long>(G, (long long)hs * n);
+    const SimResult s1 = simulate(hs_plan, hs_pred, hs, P1, c, r, true);
+    if (s1.deadlock) continue;
+    long long ms = s1.makespan;
+    int P2 = 0;
+    if (rest > 0) {
+      P2 = (int)std::min<long long>(F, (long long)rest * n);
+      const SimResult s2 = simulate(se_plan, se_pred, rest, P2, c, r, true);
+      if (s2.deadlock) continue;
+      ms = std::max(ms, s2.makespan);
+    }
+    if (best_hs < 0 || ms < best_ms) {
+      best_hs = hs;
+      best_P1 = P1;
+      best_P2 = P2;
+      best_ms = ms;
+    }
+  }
+  if (best_hs < 0) return "schedule simulation deadlocked";
+  Schedule a, b;
+  e = build_schedule(best_hs, n, false, kShift, best_P1, c, r, &a);
+  if (!e.empty()) return e;
+  if (best_P2 > 0) {
+    e = build_schedule(BH - best_hs, n, false, kSerial, best_P2, c, r, &b);
+    if (!e.empty()) return e;
+    for (size_t i = 0; i < b.tasks.size(); i += 4) b.tasks[i] += best_hs;  // those heads follow the shift heads
+  }
+  out->tasks = std::move(a.tasks);
+  out->tasks.insert(out->tasks.end(), b.tasks.begin(), b.tasks.end());
+  out->cta_off = std::move(a.cta_off);
+  const int32_t base = out->cta_off.back();
+  for (size_t i = 1; i < b.cta_off.size(); ++i) out->cta_off.push_back(base + b.cta_off[i]);
+  out->P = best_P1 + best_P2;
+  out->makespan = best_ms;
+  if (shift_heads) *shift_heads = best_hs;
+  return "";
+}
+
 int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out) {
   if (BH < 1 || n < 1 || P_max < 1 || c < 1 || r < 1) return -1;
   int best = -1, best_P = 0;

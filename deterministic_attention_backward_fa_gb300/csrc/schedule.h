@@ -39,6 +39,16 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
 // makespan, ties to fewer CTAs.
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 
+// Shift with fill (an extension beyond the pages' schedules; full mask only).
+// Whole gangs of n CTAs, as many as fit in P_max, run shift for the first
+// `shift_heads` heads; the CTAs that whole gangs leave idle run the other
+// heads with the serial schedule, each head keeping its own schedule's dQ
+// order.  shift_heads is the number of heads, among whole waves of gangs and
+// BH itself, that minimises the larger of the two parts' simulated makespans
+// (ties to more shift heads).  When no CTA is left over, or every head fits in
+// one wave, it is plain shift on choose_ctas CTAs (shift_heads = BH).
+std::string build_shift_fill(int BH, int n, int P_max, int c, int r, Schedule *out, int *shift_heads);
+
 // The deterministic schedule valid for the mask whose simulated makespan,
 // each at its own choose_ctas CTA count, is smallest (ties to the lower mode
 // number); fills its CTA count and makespan.  -1 on invalid arguments.

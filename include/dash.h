@@ -111,6 +111,11 @@ typedef struct {
                             * semaphore, and dQ = chain 0 + chain 1.  Deterministic, with a different
                             * summation order from 1.  With num_ctas = 0, shift then takes every SM
                             * instead of whole gangs.  Ignored by the atomic schedule. */
+  int shift_fill;          /* DASH_SCHED_SHIFT with one chain: 0 = the pages' shift on whole gangs of n CTAs;
+                            * 1 = shift with fill (an extension beyond the pages): the CTAs that whole gangs
+                            * leave idle run some of the heads with the serial schedule instead, as
+                            * dash_build_shift_fill lays out.  Each head keeps its own schedule's dQ order, so
+                            * the result is deterministic; those heads' bits are the serial schedule's. */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
@@ -176,6 +181,22 @@ long long dash_schedule_num_tasks(int BH, int n, int causal, dash_schedule_t sch
 dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t schedule, int P,
                                   int cost_c, int cost_r, int32_t *tasks_out,
                                   int32_t *cta_off_out, long long *makespan_out);
+
+/* Shift with fill, an extension beyond the pages' schedules (full mask only).
+ * Shift needs a whole gang of n CTAs per head (each chain waits on its gang
+ * neighbour), so on max_ctas SMs that are not a multiple of n some SMs idle.
+ * This layout runs shift for the first *shift_heads_out heads on whole gangs
+ * (CTAs 0 .. P1-1) and the other heads with the serial schedule on the CTAs
+ * that whole gangs leave over (CTAs P1 .. *ctas_out-1).  The split is the
+ * number of heads, among whole waves of gangs and BH itself, whose larger
+ * simulated makespan of the two parts is smallest (costs cost_c, cost_r; ties
+ * to more shift heads).  Without leftover CTAs, or when every head fits in one
+ * wave, it is plain shift at dash_choose_ctas' count.  tasks_out takes
+ * dash_schedule_num_tasks entries and cta_off_out max_ctas + 1.  The ranks of
+ * every head are those of its own schedule.  Host only. */
+dash_status_t dash_build_shift_fill(int BH, int n, int max_ctas, int cost_c, int cost_r, int32_t *tasks_out,
+                                    int32_t *cta_off_out, int *ctas_out, int *shift_heads_out,
+                                    long long *makespan_out);
 
 /* The CTA count the backward uses for a problem when num_ctas = 0: the
  * candidate (max_ctas, and the multiples of the schedule's gang size up to

@@ -264,6 +264,67 @@ def schedule_tables(mode: str, BH: int, n: int, causal: bool, P: int, c: int = 4
     return tasks, cta_off, sim.makespan
 
 
+def shift_fill_tables(BH: int, n: int, P_max: int, c: int = 4, r: int = 1):
+    """Shift with fill: an extension beyond the pages' schedules, full mask.
+
+    A head's shift chains each wait on a neighbour of the gang, so shift wants
+    whole gangs of n SMs, and on P_max SMs that are not a multiple of n the rest
+    idle.  Here the heads split in two: the first hs heads run shift on
+    G = (P_max // n) * n SMs, the others run the serial schedule on the
+    P_max - G SMs left over, each head keeping its own schedule's reduction
+    order.  hs ranges over whole waves of gangs (k * (P_max // n), and BH);
+    the split whose larger makespan is smallest wins, ties to more shift heads.
+    Without SMs left over, or when every head fits in one wave, this is plain
+    shift on the smallest whole number of gangs with the best makespan.
+
+    Returns (tasks, cta_off, makespan, shift_heads) like schedule_tables; the
+    serial heads are numbered after the shift heads and their CTAs come after
+    the shift CTAs.
+    """
+    per_wave = P_max // n
+    G = per_wave * n
+    F = P_max - G
+    if per_wave == 0 or F == 0 or BH <= per_wave:
+        top = min(P_max, BH * n)
+        best = None
+        for m in list(range((top // n) * n, n - 1, -n))[:16]:
+            try:
+                ms = simulate(all_chains("shift", BH, n, False), m, c, r).makespan
+            except Deadlock:
+                continue
+            if best is None or ms < best[0] or (ms == best[0] and m < best[1]):
+                best = (ms, m)
+        if best is None:
+            raise Deadlock("no whole number of gangs runs this shift schedule")
+        tasks, off, ms = schedule_tables("shift", BH, n, False, best[1], c, r)
+        return tasks, off, ms, BH
+    best = None
+    waves = -(-BH // per_wave)
+    for k in range(waves, 0, -1):
+        hs = min(BH, k * per_wave)
+        rest = BH - hs
+        P1 = min(G, hs * n)
+        try:
+            ms = simulate(all_chains("shift", hs, n, False), P1, c, r).makespan
+            P2 = 0
+            if rest:
+                P2 = min(F, rest * n)
+                ms = max(ms, simulate(all_chains("serial", rest, n, False), P2, c, r).makespan)
+        except Deadlock:
+            continue
+        if best is None or ms < best[0]:
+            best = (ms, hs, P1, P2)
+    if best is None:
+        raise Deadlock("no split runs without deadlock")
+    ms, hs, P1, P2 = best
+    tasks, off, _ = schedule_tables("shift", hs, n, False, P1, c, r)
+    if P2:
+        t2, off2, _ = schedule_tables("serial", BH - hs, n, False, P2, c, r)
+        tasks = tasks + [(bh + hs, kv, q, w) for (bh, kv, q, w) in t2]
+        off = off + [off[-1] + x for x in off2[1:]]
+    return tasks, off, ms, hs
+
+
 # Closed forms of DASH overview (zskr.cn) section 3, for m heads on n SMs.
 def t_causal_serial(m, n, c, r):
     return m * n * (c + r) + (n - 1) * r

@@ -131,6 +131,34 @@ def test_schedule_choice_is_best_simulated(BH, n, causal, c, r):
     assert dash.dash_choose_schedule(BH, n, causal, P_max, c, r) == (want, spans[want][1], best)
 
 
+FILL_CASES = [(32, 32, 152), (12, 16, 152), (4, 32, 152), (48, 16, 152), (7, 4, 10), (5, 3, 7), (9, 6, 20),
+              (16, 8, 20), (16, 128, 152)]
+
+
+@pytest.mark.parametrize("BH,n,P", FILL_CASES)
+def test_shift_fill_generator_matches_simulator(BH, n, P):
+    for c, r in ((4, 1),) if n >= 64 else ((4, 1), (1, 1), (2, 3)):   # the pure-Python simulator is slow at n = 128
+        py_tasks, py_off, py_ms, py_hs = d.shift_fill_tables(BH, n, P, c, r)
+        tasks, off, Pc, hs, ms = dash.dash_build_shift_fill(BH, n, P, c, r)
+        np.testing.assert_array_equal(tasks, np.asarray(py_tasks, dtype=np.int32).reshape(-1, 4))
+        np.testing.assert_array_equal(off, np.asarray(py_off, dtype=np.int32))
+        assert (Pc, hs, ms) == (len(py_off) - 1, py_hs, py_ms)
+
+
+def test_shift_fill_without_a_whole_gang_is_rejected():
+    with pytest.raises(d.Deadlock):
+        d.shift_fill_tables(3, 8, 5)
+    with pytest.raises(dash.DashError) as ei:
+        dash.dash_build_shift_fill(3, 8, 5)
+    assert ei.value.code == 6
+    import ctypes
+    fake = ctypes.c_void_p(1 << 20)
+    opt = dash.BwdOptions(0, 0, 0, 0, 0, None, None, None, None, None, 0, 2)
+    assert dash.lib().dash_attn_bwd_ex(*([fake] * 9), 1, 1, 128, 64, 0, 0.1, 3, ctypes.byref(opt),
+                                       ctypes.c_void_p(0)) == 1
+    assert "shift_fill" in dash.dash_last_error()
+
+
 def test_schedule_choice_rejects_bad_arguments():
     with pytest.raises(dash.DashError):
         dash.dash_choose_schedule(0, 4, False, 40)

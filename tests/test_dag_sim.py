@@ -127,3 +127,41 @@ def test_tables_flags_and_order():
             last = i == len(run) - 1 or run[i + 1][1] != kv or run[i + 1][0] != bh
             assert bool(w & d.FLAG_FIRST) == first
             assert bool(w & d.FLAG_LAST) == last
+
+
+def head_rank_map(mode, n):
+    chains = d.head_chains(mode, n, False)
+    ranks = d.head_ranks(mode, n, False, chains)
+    return {t: rk for ch, rks in zip(chains, ranks) for t, rk in zip(ch, rks)}
+
+
+@pytest.mark.parametrize("BH,n,P,c,r", [(32, 32, 152, 4, 1), (32, 32, 152, 1, 1), (7, 4, 10, 4, 1), (9, 6, 20, 2, 3),
+                                        (16, 8, 20, 1, 2), (13, 5, 12, 3, 1)])
+def test_shift_fill_split(BH, n, P, c, r):
+    # shift with fill (an extension): every tile of every head once, each head
+    # with its own schedule's ranks, CTAs within the budget, and no split of
+    # the heads, whole waves or not, with a smaller makespan
+    tasks, off, ms, hs = d.shift_fill_tables(BH, n, P, c, r)
+    assert sorted((bh, kv, q) for bh, kv, q, _ in tasks) == \
+        [(bh, kv, q) for bh in range(BH) for kv in range(n) for q in range(n)]
+    assert len(off) - 1 <= P and off[0] == 0 and off[-1] == len(tasks)
+    assert all(a <= b for a, b in zip(off, off[1:]))
+    shift_r, serial_r = head_rank_map("shift", n), head_rank_map("serial", n)
+    for bh, kv, q, w in tasks:
+        assert (w & d.RANK_MASK) == (shift_r if bh < hs else serial_r)[(kv, q)]
+    per_wave = P // n
+    if per_wave and P % n and BH > per_wave:
+        assert hs < BH or ms == makespan("shift", BH, n, False, per_wave * n, c, r)
+        brute = min(max(makespan("shift", h, n, False, min(per_wave * n, h * n), c, r),
+                        makespan("serial", BH - h, n, False, min(P % n, (BH - h) * n), c, r) if h < BH else 0)
+                    for h in range(1, BH + 1))
+        assert ms == brute
+        # the leftover CTAs only ever hold serial heads
+        first_fill_cta = min(per_wave * n, hs * n)
+        assert all(tasks[i][0] >= hs for i in range(off[first_fill_cta], len(tasks)))
+
+
+def test_shift_fill_is_plain_shift_without_leftover_ctas():
+    tasks, off, ms, hs = d.shift_fill_tables(8, 4, 16, 4, 1)   # 16 = 4 whole gangs
+    assert hs == 8
+    assert (tasks, off, ms) == d.schedule_tables("shift", 8, 4, False, 16, 4, 1)
