@@ -8,10 +8,10 @@ deterministic schedule's TFLOPS (conventional count: 10*B*H*S^2*D for a full
 mask, half of it for a causal one) and the atomic schedule gives the ratio.
 The ordered schedules are timed a second time with the optional two-chain dQ
 reduction (dq_chains = 2, a different fixed summation order); those figures go
-to `extension_two_dq_chains` and never into `value`.  For a full mask, shift is
-also timed with fill (shift_fill = 1: the SMs that whole gangs of shift chains
-leave idle run some heads in the serial order), under `extension_shift_fill`,
-never in `value`.
+to `extension_two_dq_chains` and never into `value`.  Shift and symmetric shift
+are also timed with fill (shift_fill = 1: the SMs that whole gangs of their
+chains leave idle run some heads in the serial or descending order), under
+`extension_fill`, never in `value`.
 
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -65,7 +65,7 @@ def parse():
     ap.add_argument("--no-two-chains", action="store_true",
                     help="skip timing the optional two-chain dQ reduction (dq_chains = 2)")
     ap.add_argument("--no-shift-fill", action="store_true",
-                    help="skip timing shift with fill (shift_fill = 1)")
+                    help="skip timing shift and symmetric shift with fill (shift_fill = 1)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the pages' sweep (16384 tokens, S = 512..16384, D = 64/128, both masks) "
                          "and print one JSON line per configuration instead of the bench line")
@@ -312,11 +312,11 @@ def main():
 
     results = {}
     two_chains = {}   # the optional two-chain dQ reduction (an extension beyond the pages' order)
-    fill = {}         # shift with fill (an extension beyond the pages' schedules)
+    fill = {}         # fill of the leftover SMs (an extension beyond the pages' schedules)
     launches = 0
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
     runs = [(s, 1, 0) for s in scheds] + [(s, 2, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
-    runs += [("shift", 1, 1)] if "shift" in scheds and not args.no_shift_fill else []
+    runs += [(s, 1, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
     with ClockSampler(gpu_index) as clk:
         for sched, chains, shift_fill in runs:
             evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -407,7 +407,7 @@ def main():
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
             "extension_two_dq_chains": two_chains or None,
-            "extension_shift_fill": fill or None,
+            "extension_fill": fill or None,
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,

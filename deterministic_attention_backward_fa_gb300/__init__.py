@@ -60,7 +60,7 @@ _SIGS = {
     "dash_attn_bwd_noalloc": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_schedule_num_tasks": ([_I, _I, _I, _I], ctypes.c_longlong),
     "dash_build_schedule": ([_I, _I, _I, _I, _I, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
-    "dash_build_shift_fill": ([_I] * 5 + [_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I),
+    "dash_build_shift_fill": ([_I] * 7 + [_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                                           ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
@@ -210,18 +210,20 @@ def dash_build_schedule(BH: int, n: int, causal: bool, schedule, P: int, cost_c:
     return tasks[:nt], off, int(ms.value)
 
 
-def dash_build_shift_fill(BH: int, n: int, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
-    """Host-only.  Returns (tasks int32 [N, 4], cta_off int32 [P+1], P, shift_heads, makespan)."""
-    nt = dash_schedule_num_tasks(BH, n, False, "shift")
+def dash_build_shift_fill(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
+    """Host-only.  Returns (tasks int32 [N, 4], cta_off int32 [P+1], P, shift_heads, fill schedule name or
+    None, makespan)."""
+    nt = dash_schedule_num_tasks(BH, n, causal, schedule)
     if nt < 0:
-        raise DashError(2, "schedule invalid for this n")
+        raise DashError(2, "schedule invalid for this mask / n")
     tasks = np.zeros((max(nt, 1), 4), dtype=np.int32)
     off = np.zeros(max_ctas + 1, dtype=np.int32)
-    P, hs, ms = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_longlong(0)
-    _check(lib().dash_build_shift_fill(BH, n, max_ctas, cost_c, cost_r, tasks.ctypes.data_as(ctypes.c_void_p),
-                                       off.ctypes.data_as(ctypes.c_void_p), ctypes.byref(P), ctypes.byref(hs),
-                                       ctypes.byref(ms)))
-    return tasks[:nt], off[:P.value + 1], int(P.value), int(hs.value), int(ms.value)
+    P, hs, fm, ms = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(-1), ctypes.c_longlong(0)
+    _check(lib().dash_build_shift_fill(BH, n, int(causal), _sched(schedule), max_ctas, cost_c, cost_r,
+                                       tasks.ctypes.data_as(ctypes.c_void_p), off.ctypes.data_as(ctypes.c_void_p),
+                                       ctypes.byref(P), ctypes.byref(hs), ctypes.byref(fm), ctypes.byref(ms)))
+    fill = next(k for k, v in SCHEDULES.items() if v == fm.value) if fm.value >= 0 else None
+    return tasks[:nt], off[:P.value + 1], int(P.value), int(hs.value), fill, int(ms.value)
 
 
 def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):

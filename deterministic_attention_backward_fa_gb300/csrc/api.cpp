@@ -238,7 +238,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (opt && (opt->dq_chains < 0 || opt->dq_chains > 2)) return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
   const int chains = (mode != DASH_SCHED_ATOMIC && opt && opt->dq_chains == 2) ? 2 : 1;
   if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1)) return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
-  const bool fill = mode == DASH_SCHED_SHIFT && chains == 1 && opt && opt->shift_fill == 1;
+  const bool fill = (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT) && chains == 1 && opt &&
+                    opt->shift_fill == 1;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -291,7 +292,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       }
       dash::Schedule sch;
       if (fill) {
-        why = dash::build_shift_fill(BH, n, want ? want : sms, c, r, &sch, nullptr);
+        why = dash::build_fill(BH, n, causal != 0, mode, want ? want : sms, c, r, &sch, nullptr, nullptr);
         Puse = sch.P;
       } else {
         why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch);
@@ -540,19 +541,23 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
   return DASH_OK;
 }
 
-dash_status_t dash_build_shift_fill(int BH, int n, int max_ctas, int cost_c, int cost_r, int32_t *tasks_out,
-                                    int32_t *cta_off_out, int *ctas_out, int *shift_heads_out, long long *makespan_out) {
+dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int cost_c,
+                                    int cost_r, int32_t *tasks_out, int32_t *cta_off_out, int *ctas_out,
+                                    int *shift_heads_out, int *fill_schedule_out, long long *makespan_out) {
   if (!tasks_out || !cta_off_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
-  std::string why = dash::check_mode(dash::kShift, n, false);
+  if (schedule != DASH_SCHED_SHIFT && schedule != DASH_SCHED_SYMMETRIC_SHIFT)
+    return fail(DASH_ERR_UNSUPPORTED, "fill applies to shift and symmetric shift only");
+  std::string why = dash::check_mode((int)schedule, n, causal != 0);
   if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
   dash::Schedule s;
-  int hs = 0;
-  why = dash::build_shift_fill(BH, n, max_ctas, cost_c, cost_r, &s, &hs);
+  int hs = 0, fm = -1;
+  why = dash::build_fill(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r, &s, &hs, &fm);
   if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
   std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
   std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
   if (ctas_out) *ctas_out = s.P;
   if (shift_heads_out) *shift_heads_out = hs;
+  if (fill_schedule_out) *fill_schedule_out = fm;
   if (makespan_out) *makespan_out = s.makespan;
   return DASH_OK;
 }

@@ -293,49 +293,65 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
   return best;
 }
 
-std::string build_shift_fill(int BH, int n, int P_max, int c, int r, Schedule *out, int *shift_heads) {
-  std::string e = check_mode(kShift, n, false);
+std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, int r, Schedule *out,
+                       int *shift_heads, int *fill_mode) {
+  if (mode != kShift && mode != kSymmetricShift) return "fill applies to shift and symmetric shift only";
+  std::string e = check_mode(mode, n, causal);
   if (!e.empty()) return e;
   if (BH < 1 || P_max < 1 || c < 1 || r < 1) return "BH, P and the costs must be >= 1";
-  const int per_wave = P_max / n;  // heads whose gangs fit side by side
-  const int G = per_wave * n, F = P_max - G;
+  const int gang = chains_per_head(mode, n);
+  const int per_wave = P_max / gang;  // heads whose gangs fit side by side
+  const int G = per_wave * gang, F = P_max - G;
+  if (fill_mode) *fill_mode = -1;
   if (per_wave == 0 || F == 0 || BH <= per_wave) {
-    const int P = choose_ctas(BH, n, false, kShift, P_max, c, r);
+    const int P = choose_ctas(BH, n, causal, mode, P_max, c, r);
     if (P < 1) return "no CTA count runs this schedule without deadlock";
     if (shift_heads) *shift_heads = BH;
-    return build_schedule(BH, n, false, kShift, P, c, r, out);
+    return build_schedule(BH, n, causal, mode, P, c, r, out);
   }
-  const HeadPlan hs_plan = head_plan(kShift, n, false), se_plan = head_plan(kSerial, n, false);
-  const std::vector<int> hs_pred = head_pred(hs_plan, n), se_pred = head_pred(se_plan, n);
-  int best_hs = -1, best_P1 = 0, best_P2 = 0;
+  const HeadPlan sh_plan = head_plan(mode, n, causal);
+  const std::vector<int> sh_pred = head_pred(sh_plan, n);
+  std::vector<int> fill_modes = {kSerial};
+  if (causal) fill_modes.push_back(kDescendingQ);
+  std::vector<HeadPlan> f_plan;
+  std::vector<std::vector<int>> f_pred;
+  for (int m : fill_modes) {
+    f_plan.push_back(head_plan(m, n, causal));
+    f_pred.push_back(head_pred(f_plan.back(), n));
+  }
+  int best_hs = -1, best_P1 = 0, best_P2 = 0, best_fm = -1;
   long long best_ms = 0;
   const int waves = (BH + per_wave - 1) / per_wave;
   for (int k = waves; k >= 1; --k) {  // more shift heads first, so that ties keep them
     const int hs = std::min(BH, k * per_wave), rest = BH - hs;
-    const int P1 = (int)std::min<long long>(G, (long long)hs * n);
-    const SimResult s1 = simulate(hs_plan, hs_pred, hs, P1, c, r, true);
+    const int P1 = (int)std::min<long long>(G, (long long)hs * gang);
+    const SimResult s1 = simulate(sh_plan, sh_pred, hs, P1, c, r, true);
     if (s1.deadlock) continue;
-    long long ms = s1.makespan;
-    int P2 = 0;
-    if (rest > 0) {
-      P2 = (int)std::min<long long>(F, (long long)rest * n);
-      const SimResult s2 = simulate(se_plan, se_pred, rest, P2, c, r, true);
-      if (s2.deadlock) continue;
-      ms = std::max(ms, s2.makespan);
-    }
-    if (best_hs < 0 || ms < best_ms) {
-      best_hs = hs;
-      best_P1 = P1;
-      best_P2 = P2;
-      best_ms = ms;
+    for (size_t f = 0; f < fill_modes.size(); ++f) {
+      long long ms = s1.makespan;
+      int P2 = 0;
+      if (rest > 0) {
+        P2 = (int)std::min<long long>(F, (long long)rest * n);
+        const SimResult s2 = simulate(f_plan[f], f_pred[f], rest, P2, c, r, true);
+        if (s2.deadlock) continue;
+        ms = std::max(ms, s2.makespan);
+      }
+      if (best_hs < 0 || ms < best_ms) {
+        best_hs = hs;
+        best_P1 = P1;
+        best_P2 = P2;
+        best_fm = rest > 0 ? fill_modes[f] : -1;
+        best_ms = ms;
+      }
+      if (rest == 0) break;
     }
   }
   if (best_hs < 0) return "schedule simulation deadlocked";
   Schedule a, b;
-  e = build_schedule(best_hs, n, false, kShift, best_P1, c, r, &a);
+  e = build_schedule(best_hs, n, causal, mode, best_P1, c, r, &a);
   if (!e.empty()) return e;
   if (best_P2 > 0) {
-    e = build_schedule(BH - best_hs, n, false, kSerial, best_P2, c, r, &b);
+    e = build_schedule(BH - best_hs, n, causal, best_fm, best_P2, c, r, &b);
     if (!e.empty()) return e;
     for (size_t i = 0; i < b.tasks.size(); i += 4) b.tasks[i] += best_hs;  // those heads follow the shift heads
   }
@@ -347,6 +363,7 @@ std::string build_shift_fill(int BH, int n, int P_max, int c, int r, Schedule *o
   out->P = best_P1 + best_P2;
   out->makespan = best_ms;
   if (shift_heads) *shift_heads = best_hs;
+  if (fill_mode) *fill_mode = best_fm;
   return "";
 }
 

@@ -39,15 +39,18 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
 // makespan, ties to fewer CTAs.
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 
-// Shift with fill (an extension beyond the pages' schedules; full mask only).
-// Whole gangs of n CTAs, as many as fit in P_max, run shift for the first
-// `shift_heads` heads; the CTAs that whole gangs leave idle run the other
-// heads with the serial schedule, each head keeping its own schedule's dQ
-// order.  shift_heads is the number of heads, among whole waves of gangs and
-// BH itself, that minimises the larger of the two parts' simulated makespans
-// (ties to more shift heads).  When no CTA is left over, or every head fits in
-// one wave, it is plain shift on choose_ctas CTAs (shift_heads = BH).
-std::string build_shift_fill(int BH, int n, int P_max, int c, int r, Schedule *out, int *shift_heads);
+// Fill (an extension beyond the pages' schedules) for shift (full mask) and
+// symmetric shift (causal): whole gangs of CTAs, as many as fit in P_max, run
+// `mode` for the first `shift_heads` heads; the CTAs that whole gangs leave
+// idle run the other heads with a fill schedule (serial; for a causal mask
+// serial or descending_q), each head keeping its own schedule's dQ order.
+// The split is the number of heads, among whole waves of gangs and BH itself,
+// and the fill schedule whose larger simulated makespan of the two parts is
+// smallest (ties to more shift heads, then to serial).  When no CTA is left
+// over, or every head fits in one wave, it is plain `mode` on choose_ctas CTAs
+// (shift_heads = BH, fill_mode = -1).
+std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, int r, Schedule *out,
+                       int *shift_heads, int *fill_mode);
 
 // The deterministic schedule valid for the mask whose simulated makespan,
 // each at its own choose_ctas CTA count, is smallest (ties to the lower mode

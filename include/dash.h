@@ -111,11 +111,13 @@ typedef struct {
                             * semaphore, and dQ = chain 0 + chain 1.  Deterministic, with a different
                             * summation order from 1.  With num_ctas = 0, shift then takes every SM
                             * instead of whole gangs.  Ignored by the atomic schedule. */
-  int shift_fill;          /* DASH_SCHED_SHIFT with one chain: 0 = the pages' shift on whole gangs of n CTAs;
-                            * 1 = shift with fill (an extension beyond the pages): the CTAs that whole gangs
-                            * leave idle run some of the heads with the serial schedule instead, as
-                            * dash_build_shift_fill lays out.  Each head keeps its own schedule's dQ order, so
-                            * the result is deterministic; those heads' bits are the serial schedule's. */
+  int shift_fill;          /* DASH_SCHED_SHIFT and DASH_SCHED_SYMMETRIC_SHIFT with one chain: 0 = the pages'
+                            * schedule; 1 = with fill (an extension beyond the pages): whole gangs of CTAs run
+                            * the schedule for most heads, and the CTAs they leave idle run the other heads
+                            * with a fill schedule (serial or descending_q), as dash_build_shift_fill lays out.
+                            * Each head keeps its own schedule's dQ order, so the result is deterministic;
+                            * the filled heads' bits are the fill schedule's.  num_ctas, if set, is the CTA
+                            * budget. */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
@@ -182,21 +184,25 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
                                   int cost_c, int cost_r, int32_t *tasks_out,
                                   int32_t *cta_off_out, long long *makespan_out);
 
-/* Shift with fill, an extension beyond the pages' schedules (full mask only).
- * Shift needs a whole gang of n CTAs per head (each chain waits on its gang
- * neighbour), so on max_ctas SMs that are not a multiple of n some SMs idle.
- * This layout runs shift for the first *shift_heads_out heads on whole gangs
- * (CTAs 0 .. P1-1) and the other heads with the serial schedule on the CTAs
- * that whole gangs leave over (CTAs P1 .. *ctas_out-1).  The split is the
- * number of heads, among whole waves of gangs and BH itself, whose larger
- * simulated makespan of the two parts is smallest (costs cost_c, cost_r; ties
- * to more shift heads).  Without leftover CTAs, or when every head fits in one
- * wave, it is plain shift at dash_choose_ctas' count.  tasks_out takes
- * dash_schedule_num_tasks entries and cta_off_out max_ctas + 1.  The ranks of
- * every head are those of its own schedule.  Host only. */
-dash_status_t dash_build_shift_fill(int BH, int n, int max_ctas, int cost_c, int cost_r, int32_t *tasks_out,
-                                    int32_t *cta_off_out, int *ctas_out, int *shift_heads_out,
-                                    long long *makespan_out);
+/* Fill, an extension beyond the pages' schedules, for DASH_SCHED_SHIFT (full
+ * mask) and DASH_SCHED_SYMMETRIC_SHIFT (causal).  Each of their chains waits
+ * on a neighbour in its head's gang (n chains for shift, n/2 for symmetric
+ * shift), so on max_ctas SMs that are not a multiple of the gang some SMs
+ * idle or a split gang stalls.  This layout runs `schedule` for the first
+ * *shift_heads_out heads on whole gangs (CTAs 0 .. P1-1) and the other heads
+ * with a fill schedule on the CTAs that whole gangs leave over (CTAs P1 ..
+ * *ctas_out-1): serial, or for a causal mask serial or descending_q
+ * (*fill_schedule_out; -1 when no head is filled).  The split is the number
+ * of heads, among whole waves of gangs and BH itself, and the fill schedule
+ * whose larger simulated makespan of the two parts is smallest (costs cost_c,
+ * cost_r; ties to more shift heads, then to serial).  Without leftover CTAs,
+ * or when every head fits in one wave, it is plain `schedule` at
+ * dash_choose_ctas' count.  tasks_out takes dash_schedule_num_tasks entries
+ * and cta_off_out max_ctas + 1.  The ranks of every head are those of its own
+ * schedule.  Host only. */
+dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int cost_c,
+                                    int cost_r, int32_t *tasks_out, int32_t *cta_off_out, int *ctas_out,
+                                    int *shift_heads_out, int *fill_schedule_out, long long *makespan_out);
 
 /* The CTA count the backward uses for a problem when num_ctas = 0: the
  * candidate (max_ctas, and the multiples of the schedule's gang size up to

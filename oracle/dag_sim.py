@@ -264,65 +264,81 @@ def schedule_tables(mode: str, BH: int, n: int, causal: bool, P: int, c: int = 4
     return tasks, cta_off, sim.makespan
 
 
-def shift_fill_tables(BH: int, n: int, P_max: int, c: int = 4, r: int = 1):
-    """Shift with fill: an extension beyond the pages' schedules, full mask.
+def fill_tables(mode: str, BH: int, n: int, causal: bool, P_max: int, c: int = 4, r: int = 1):
+    """Fill: an extension beyond the pages' schedules, for shift (full mask) and
+    symmetric shift (causal).
 
-    A head's shift chains each wait on a neighbour of the gang, so shift wants
-    whole gangs of n SMs, and on P_max SMs that are not a multiple of n the rest
-    idle.  Here the heads split in two: the first hs heads run shift on
-    G = (P_max // n) * n SMs, the others run the serial schedule on the
-    P_max - G SMs left over, each head keeping its own schedule's reduction
-    order.  hs ranges over whole waves of gangs (k * (P_max // n), and BH);
-    the split whose larger makespan is smallest wins, ties to more shift heads.
-    Without SMs left over, or when every head fits in one wave, this is plain
-    shift on the smallest whole number of gangs with the best makespan.
+    A head's chains each wait on a neighbour in the head's gang (n chains for
+    shift, n/2 for symmetric shift), so these schedules want whole gangs of
+    SMs, and on P_max SMs that are not a multiple of the gang the rest idle.
+    Here the heads split in two: the first hs heads run `mode` on
+    G = (P_max // gang) * gang SMs, the others run a fill schedule on the
+    P_max - G SMs left over (serial; for a causal mask serial or
+    descending_q), each head keeping its own schedule's reduction order.
+    hs ranges over whole waves of gangs (k * (P_max // gang), and BH); the
+    split and fill schedule whose larger makespan is smallest win, ties to
+    more shift heads, then to serial.  Without SMs left over, or when every
+    head fits in one wave, this is plain `mode` on the CTA count that the
+    library's CTA choice takes (for shift the smallest whole number of gangs
+    with the best makespan; for symmetric shift also P_max itself).
 
-    Returns (tasks, cta_off, makespan, shift_heads) like schedule_tables; the
-    serial heads are numbered after the shift heads and their CTAs come after
-    the shift CTAs.
+    Returns (tasks, cta_off, makespan, shift_heads, fill_mode or None) like
+    schedule_tables; the filled heads are numbered after the others and
+    their CTAs come after theirs.
     """
-    per_wave = P_max // n
-    G = per_wave * n
+    check_mode(mode, n, causal)
+    if mode not in ("shift", "symmetric_shift"):
+        raise ScheduleError("fill applies to shift and symmetric shift only")
+    gang = n // 2 if mode == "symmetric_shift" else n
+    per_wave = P_max // gang
+    G = per_wave * gang
     F = P_max - G
     if per_wave == 0 or F == 0 or BH <= per_wave:
-        top = min(P_max, BH * n)
+        top = min(P_max, BH * gang)
+        cands = list(range((top // gang) * gang, gang - 1, -gang))
+        if mode == "symmetric_shift":   # the CTA choice also offers the full count
+            cands = [top] + [m for m in cands if m != top][:15]
         best = None
-        for m in list(range((top // n) * n, n - 1, -n))[:16]:
+        for m in cands[:16]:
             try:
-                ms = simulate(all_chains("shift", BH, n, False), m, c, r).makespan
+                ms = simulate(all_chains(mode, BH, n, causal), m, c, r).makespan
             except Deadlock:
                 continue
             if best is None or ms < best[0] or (ms == best[0] and m < best[1]):
                 best = (ms, m)
         if best is None:
-            raise Deadlock("no whole number of gangs runs this shift schedule")
-        tasks, off, ms = schedule_tables("shift", BH, n, False, best[1], c, r)
-        return tasks, off, ms, BH
+            raise Deadlock("no CTA count runs this schedule without deadlock")
+        tasks, off, ms = schedule_tables(mode, BH, n, causal, best[1], c, r)
+        return tasks, off, ms, BH, None
+    fills = ("serial", "descending_q") if causal else ("serial",)
     best = None
-    waves = -(-BH // per_wave)
-    for k in range(waves, 0, -1):
+    for k in range(-(-BH // per_wave), 0, -1):
         hs = min(BH, k * per_wave)
         rest = BH - hs
-        P1 = min(G, hs * n)
+        P1 = min(G, hs * gang)
         try:
-            ms = simulate(all_chains("shift", hs, n, False), P1, c, r).makespan
-            P2 = 0
-            if rest:
-                P2 = min(F, rest * n)
-                ms = max(ms, simulate(all_chains("serial", rest, n, False), P2, c, r).makespan)
+            ms1 = simulate(all_chains(mode, hs, n, causal), P1, c, r).makespan
         except Deadlock:
             continue
-        if best is None or ms < best[0]:
-            best = (ms, hs, P1, P2)
+        for fm in (fills if rest else (None,)):
+            ms, P2 = ms1, 0
+            if rest:
+                P2 = min(F, rest * n)
+                try:
+                    ms = max(ms, simulate(all_chains(fm, rest, n, causal), P2, c, r).makespan)
+                except Deadlock:
+                    continue
+            if best is None or ms < best[0]:
+                best = (ms, hs, P1, P2, fm)
     if best is None:
         raise Deadlock("no split runs without deadlock")
-    ms, hs, P1, P2 = best
-    tasks, off, _ = schedule_tables("shift", hs, n, False, P1, c, r)
+    ms, hs, P1, P2, fm = best
+    tasks, off, _ = schedule_tables(mode, hs, n, causal, P1, c, r)
     if P2:
-        t2, off2, _ = schedule_tables("serial", BH - hs, n, False, P2, c, r)
+        t2, off2, _ = schedule_tables(fm, BH - hs, n, causal, P2, c, r)
         tasks = tasks + [(bh + hs, kv, q, w) for (bh, kv, q, w) in t2]
         off = off + [off[-1] + x for x in off2[1:]]
-    return tasks, off, ms, hs
+    return tasks, off, ms, hs, fm
 
 
 # Closed forms of DASH overview (zskr.cn) section 3, for m heads on n SMs.

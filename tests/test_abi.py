@@ -131,26 +131,33 @@ def test_schedule_choice_is_best_simulated(BH, n, causal, c, r):
     assert dash.dash_choose_schedule(BH, n, causal, P_max, c, r) == (want, spans[want][1], best)
 
 
-FILL_CASES = [(32, 32, 152), (12, 16, 152), (4, 32, 152), (48, 16, 152), (7, 4, 10), (5, 3, 7), (9, 6, 20),
-              (16, 8, 20), (16, 128, 152)]
+FILL_CASES = [("shift", False, 32, 32, 152), ("shift", False, 12, 16, 152), ("shift", False, 4, 32, 152),
+              ("shift", False, 48, 16, 152), ("shift", False, 7, 4, 10), ("shift", False, 5, 3, 7),
+              ("shift", False, 9, 6, 20), ("shift", False, 16, 8, 20), ("shift", False, 16, 128, 152),
+              ("symmetric_shift", True, 32, 64, 152), ("symmetric_shift", True, 64, 16, 152),
+              ("symmetric_shift", True, 9, 8, 14), ("symmetric_shift", True, 5, 6, 11),
+              ("symmetric_shift", True, 16, 8, 10), ("symmetric_shift", True, 16, 128, 152)]
 
 
-@pytest.mark.parametrize("BH,n,P", FILL_CASES)
-def test_shift_fill_generator_matches_simulator(BH, n, P):
-    for c, r in ((4, 1),) if n >= 64 else ((4, 1), (1, 1), (2, 3)):   # the pure-Python simulator is slow at n = 128
-        py_tasks, py_off, py_ms, py_hs = d.shift_fill_tables(BH, n, P, c, r)
-        tasks, off, Pc, hs, ms = dash.dash_build_shift_fill(BH, n, P, c, r)
+@pytest.mark.parametrize("mode,causal,BH,n,P", FILL_CASES)
+def test_fill_generator_matches_simulator(mode, causal, BH, n, P):
+    for c, r in ((4, 1),) if n >= 64 else ((4, 1), (1, 1), (1, 3)):   # the pure-Python simulator is slow at large n
+        py_tasks, py_off, py_ms, py_hs, py_fill = d.fill_tables(mode, BH, n, causal, P, c, r)
+        tasks, off, Pc, hs, fill, ms = dash.dash_build_shift_fill(BH, n, causal, mode, P, c, r)
         np.testing.assert_array_equal(tasks, np.asarray(py_tasks, dtype=np.int32).reshape(-1, 4))
         np.testing.assert_array_equal(off, np.asarray(py_off, dtype=np.int32))
-        assert (Pc, hs, ms) == (len(py_off) - 1, py_hs, py_ms)
+        assert (Pc, hs, fill, ms) == (len(py_off) - 1, py_hs, py_fill, py_ms)
 
 
-def test_shift_fill_without_a_whole_gang_is_rejected():
+def test_fill_rejections():
     with pytest.raises(d.Deadlock):
-        d.shift_fill_tables(3, 8, 5)
+        d.fill_tables("shift", 3, 8, False, 5)
     with pytest.raises(dash.DashError) as ei:
-        dash.dash_build_shift_fill(3, 8, 5)
+        dash.dash_build_shift_fill(3, 8, False, "shift", 5)
     assert ei.value.code == 6
+    with pytest.raises(dash.DashError) as ei:   # fill applies to the cyclic schedules only
+        dash.dash_build_shift_fill(4, 8, False, "serial", 40)
+    assert ei.value.code == 2
     import ctypes
     fake = ctypes.c_void_p(1 << 20)
     opt = dash.BwdOptions(0, 0, 0, 0, 0, None, None, None, None, None, 0, 2)

@@ -129,39 +129,44 @@ def test_tables_flags_and_order():
             assert bool(w & d.FLAG_LAST) == last
 
 
-def head_rank_map(mode, n):
-    chains = d.head_chains(mode, n, False)
-    ranks = d.head_ranks(mode, n, False, chains)
+def head_rank_map(mode, n, causal):
+    chains = d.head_chains(mode, n, causal)
+    ranks = d.head_ranks(mode, n, causal, chains)
     return {t: rk for ch, rks in zip(chains, ranks) for t, rk in zip(ch, rks)}
 
 
-@pytest.mark.parametrize("BH,n,P,c,r", [(32, 32, 152, 4, 1), (32, 32, 152, 1, 1), (7, 4, 10, 4, 1), (9, 6, 20, 2, 3),
-                                        (16, 8, 20, 1, 2), (13, 5, 12, 3, 1)])
-def test_shift_fill_split(BH, n, P, c, r):
-    # shift with fill (an extension): every tile of every head once, each head
-    # with its own schedule's ranks, CTAs within the budget, and no split of
-    # the heads, whole waves or not, with a smaller makespan
-    tasks, off, ms, hs = d.shift_fill_tables(BH, n, P, c, r)
-    assert sorted((bh, kv, q) for bh, kv, q, _ in tasks) == \
-        [(bh, kv, q) for bh in range(BH) for kv in range(n) for q in range(n)]
+@pytest.mark.parametrize("mode,causal,BH,n,P,c,r", [
+    ("shift", False, 32, 32, 152, 4, 1), ("shift", False, 32, 32, 152, 1, 1), ("shift", False, 7, 4, 10, 4, 1),
+    ("shift", False, 9, 6, 20, 2, 3), ("shift", False, 16, 8, 20, 1, 2), ("shift", False, 13, 5, 12, 3, 1),
+    ("symmetric_shift", True, 16, 8, 10, 4, 1), ("symmetric_shift", True, 16, 8, 10, 1, 1),
+    ("symmetric_shift", True, 11, 6, 14, 1, 3), ("symmetric_shift", True, 12, 16, 36, 2, 1)])
+def test_fill_split(mode, causal, BH, n, P, c, r):
+    # fill (an extension): every tile of every head once, each head with its
+    # own schedule's ranks, CTAs within the budget, the leftover CTAs holding
+    # only filled heads, and no split of the heads (whole waves or not) or
+    # fill schedule with a smaller makespan
+    tasks, off, ms, hs, fm = d.fill_tables(mode, BH, n, causal, P, c, r)
+    tiles = [(kv, q) for kv in range(n) for q in range(n) if not causal or q >= kv]
+    assert sorted((bh, kv, q) for bh, kv, q, _ in tasks) == [(bh, kv, q) for bh in range(BH) for kv, q in tiles]
     assert len(off) - 1 <= P and off[0] == 0 and off[-1] == len(tasks)
     assert all(a <= b for a, b in zip(off, off[1:]))
-    shift_r, serial_r = head_rank_map("shift", n), head_rank_map("serial", n)
+    own = head_rank_map(mode, n, causal)
+    other = head_rank_map(fm, n, causal) if fm else None
     for bh, kv, q, w in tasks:
-        assert (w & d.RANK_MASK) == (shift_r if bh < hs else serial_r)[(kv, q)]
-    per_wave = P // n
-    if per_wave and P % n and BH > per_wave:
-        assert hs < BH or ms == makespan("shift", BH, n, False, per_wave * n, c, r)
-        brute = min(max(makespan("shift", h, n, False, min(per_wave * n, h * n), c, r),
-                        makespan("serial", BH - h, n, False, min(P % n, (BH - h) * n), c, r) if h < BH else 0)
-                    for h in range(1, BH + 1))
-        assert ms == brute
-        # the leftover CTAs only ever hold serial heads
-        first_fill_cta = min(per_wave * n, hs * n)
-        assert all(tasks[i][0] >= hs for i in range(off[first_fill_cta], len(tasks)))
+        assert (w & d.RANK_MASK) == (own if bh < hs else other)[(kv, q)]
+    gang = n // 2 if mode == "symmetric_shift" else n
+    per_wave, F = P // gang, P % gang
+    assert per_wave and F and BH > per_wave, "the case must exercise the fill"
+    fills = ("serial", "descending_q") if causal else ("serial",)
+    brute = min(max(makespan(mode, h, n, causal, min(per_wave * gang, h * gang), c, r),
+                    min(makespan(f, BH - h, n, causal, min(F, (BH - h) * n), c, r) for f in fills) if h < BH else 0)
+                for h in range(1, BH + 1))
+    assert ms == brute
+    first_fill_cta = min(per_wave * gang, hs * gang)
+    assert all(tasks[i][0] >= hs for i in range(off[first_fill_cta], len(tasks)))
 
 
-def test_shift_fill_is_plain_shift_without_leftover_ctas():
-    tasks, off, ms, hs = d.shift_fill_tables(8, 4, 16, 4, 1)   # 16 = 4 whole gangs
-    assert hs == 8
+def test_fill_is_plain_shift_without_leftover_ctas():
+    tasks, off, ms, hs, fm = d.fill_tables("shift", 8, 4, False, 16, 4, 1)   # 16 = 4 whole gangs
+    assert (hs, fm) == (8, None)
     assert (tasks, off, ms) == d.schedule_tables("shift", 8, 4, False, 16, 4, 1)

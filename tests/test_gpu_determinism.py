@@ -126,18 +126,19 @@ def test_supplied_table_equal_to_generated_gives_same_bits():
         assert torch.equal(a, b)
 
 
-def test_shift_fill_bit_identical_across_runs():
-    # shift with fill (an extension): each head's order is its own schedule's
-    w = workloads.WORKLOADS["full_s4096_d128"]
+@pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
+def test_fill_bit_identical_across_runs(wname, sched):
+    # fill (an extension): each head's order is its own schedule's
+    w = workloads.WORKLOADS[wname]
     P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
-    first = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, "shift", dq_accum=True, tile=w.tile,
+    first = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, dq_accum=True, tile=w.tile,
                           shift_fill=1)
     outs = [torch.empty_like(x) for x in first]
     same = True
     for _ in range(RUNS - 1):
-        dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, outs[0], outs[1], outs[2], w.causal, P.scale, "shift",
+        dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, outs[0], outs[1], outs[2], w.causal, P.scale, sched,
                               tile=w.tile, dq_accum_out=outs[3], shift_fill=1)
         same = same and all(torch.equal(a, b) for a, b in zip(outs, first))
     dash.dash_sync_status()
-    assert same, f"shift with fill is not bit-identical across {RUNS} runs"
+    assert same, f"{wname}: {sched} with fill is not bit-identical across {RUNS} runs"

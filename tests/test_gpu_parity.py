@@ -90,31 +90,36 @@ def test_two_dq_chains_match_oracle(B, H, S, D, causal, tile):
             assert_close(f"{sched} two chains {name}", x, r)
 
 
-def test_shift_fill_heads_equal_their_own_schedules():
-    # shift with fill (an extension): the heads on whole gangs give plain
-    # shift's bits, the heads on the leftover CTAs plain serial's; the last
-    # head is also checked against the oracle
-    w = workloads.WORKLOADS["full_s4096_d128"]
+@pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
+def test_fill_heads_equal_their_own_schedules(wname, sched):
+    # fill (an extension): the heads on whole gangs give the plain schedule's
+    # bits, the heads on the leftover CTAs the fill schedule's; the last head
+    # is also checked against the row-wise oracle on sampled rows
+    w = workloads.WORKLOADS[wname]
     BH, n = w.B * w.H, w.S // w.tile
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    _, _, ctas, hs, _ = dash.dash_build_shift_fill(BH, n, sms)
+    _, _, ctas, hs, fill_sched, _ = dash.dash_build_shift_fill(BH, n, w.causal, sched, sms)
     P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
-    run = lambda sched, **kw: [x.reshape(BH, w.S, w.D) for x in dash.attn_bwd(
-        P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile, dq_accum=True, **kw)]
-    fill, shift, serial = run("shift", shift_fill=1), run("shift"), run("serial")
+    run = lambda s_, **kw: [x.reshape(BH, w.S, w.D) for x in dash.attn_bwd(
+        P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, s_, tile=w.tile, dq_accum=True, **kw)]
+    fill, plain = run(sched, shift_fill=1), run(sched)
     dash.dash_sync_status()
-    for a, s_, r_ in zip(fill, shift, serial):
-        assert torch.equal(a[:hs], s_[:hs])
-        assert torch.equal(a[hs:], r_[hs:])
-    print(f"shift with fill on {sms} SMs: {hs} of {BH} heads by shift, {ctas} CTAs")
+    for a, b in zip(fill, plain):
+        assert torch.equal(a[:hs], b[:hs])
+    if fill_sched:
+        other = run(fill_sched)
+        dash.dash_sync_status()
+        for a, b in zip(fill, other):
+            assert torch.equal(a[hs:], b[hs:])
+    print(f"{wname} {sched} with fill on {sms} SMs: {hs} of {BH} heads, the rest {fill_sched}, {ctas} CTAs")
     q, k, v, do = P.f64
-    b, h = w.B - 1, w.H - 1
-    sl = (slice(b, b + 1), slice(h, h + 1))
-    oh, lh = o[b, h].double().cpu().numpy(), lse[b, h].double().cpu().numpy()
-    ref = A.backward(q[sl], k[sl], v[sl], oh[None, None], do[sl], lh[None, None], w.causal, P.scale)
+    b_, h_ = w.B - 1, w.H - 1
+    rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1})
+    oh, lh = o[b_, h_].double().cpu().numpy(), lse[b_, h_].double().cpu().numpy()
+    ref = A.backward_rows(q[b_, h_], k[b_, h_], v[b_, h_], oh, do[b_, h_], lh, w.causal, P.scale, rows)
     for name, x, r in zip(("dQ", "dK", "dV"), fill[:3], ref):
-        assert_close(f"shift with fill {name}[{b},{h}]", x[BH - 1], r[0, 0])
+        assert_close(f"{sched} with fill {name}[{b_},{h_}] rows", x[BH - 1][rows], r)
 
 
 LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
