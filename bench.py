@@ -230,31 +230,36 @@ def run_sweep(args, dash):
         q, k, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
         o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-        res = {}
+        res, fill = {}, {}
+        runs = [(s, 0) for s in w.schedules]
+        runs += [(s, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
         with ClockSampler(0) as clk:
-            for sched in w.schedules:
+            for sched, shift_fill in runs:
                 for _ in range(args.warmup):
                     flush.fill_(1)
-                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile)
+                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                          shift_fill=shift_fill)
                 dash.dash_sync_status()
                 ms = []
                 for _ in range(args.steps):
                     flush.fill_(1)
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile)
+                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                          shift_fill=shift_fill)
                     b.record(stream)
                     b.synchronize()
                     ms.append(a.elapsed_time(b))
                 dash.dash_sync_status()
-                res[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
+                (fill if shift_fill else res)[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
         det = {s: t for s, t in res.items() if s != "atomic"}
         best = max(det, key=det.get)
         print(json.dumps({"sweep": "pages_16k_tokens", "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
                           "mask": "causal" if w.causal else "full", "tile": w.tile, "unit": "TFLOPS",
                           "statistic": f"median of {args.steps} steps", "schedules": res,
                           "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
-                          "ratio_vs_atomic": det[best] / res["atomic"], "clocks": clk.summary()}), flush=True)
+                          "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
+                          "clocks": clk.summary()}), flush=True)
         del q, k, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
 
