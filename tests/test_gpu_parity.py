@@ -90,8 +90,9 @@ def test_two_dq_chains_match_oracle(B, H, S, D, causal, tile):
             assert_close(f"{sched} two chains {name}", x, r)
 
 
+@pytest.mark.parametrize("chains", [1, 2])
 @pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
-def test_fill_heads_equal_their_own_schedules(wname, sched):
+def test_fill_heads_equal_their_own_schedules(wname, sched, chains):
     # fill (an extension): the heads on whole gangs give the plain schedule's
     # bits, the heads on the leftover CTAs the fill schedule's; the last head
     # is also checked against the row-wise oracle on sampled rows
@@ -102,7 +103,7 @@ def test_fill_heads_equal_their_own_schedules(wname, sched):
     P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
     run = lambda s_, **kw: [x.reshape(BH, w.S, w.D) for x in dash.attn_bwd(
-        P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, s_, tile=w.tile, dq_accum=True, **kw)]
+        P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, s_, tile=w.tile, dq_accum=True, dq_chains=chains, **kw)]
     fill, plain = run(sched, shift_fill=1), run(sched)
     dash.dash_sync_status()
     for a, b in zip(fill, plain):
