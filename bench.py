@@ -218,6 +218,16 @@ def run_reference(args, rank, world):
     return 0
 
 
+def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best):
+    """The library's runtime schedule choice with task costs fitted to this run's atomic and
+    serial times, against the schedule measured best."""
+    BH, n = w.B * w.H, w.S // w.tile
+    c, r = dash.dash_fit_costs(BH, n, w.causal, sms, atomic_ms, serial_ms)
+    chosen, ctas, _ = dash.dash_choose_schedule(BH, n, w.causal, sms, c, r)
+    return {"cost_c": c, "cost_r": r, "chosen": chosen, "ctas": ctas, "measured_best": measured_best,
+            "agrees": chosen == measured_best}
+
+
 def run_sweep(args, dash):
     """The pages' sweep, one GPU: every configuration and every schedule valid for its mask,
     timed like the bench line (event-timed steps, L2 flushed between steps)."""
@@ -254,12 +264,14 @@ def run_sweep(args, dash):
                 (fill if shift_fill else res)[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
         det = {s: t for s, t in res.items() if s != "atomic"}
         best = max(det, key=det.get)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        choice = runtime_choice(dash, w, sms, 1.0 / res["atomic"], 1.0 / res["serial"], best)
         print(json.dumps({"sweep": "pages_16k_tokens", "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
                           "mask": "causal" if w.causal else "full", "tile": w.tile, "unit": "TFLOPS",
                           "statistic": f"median of {args.steps} steps", "schedules": res,
                           "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
                           "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
-                          "clocks": clk.summary()}), flush=True)
+                          "runtime_choice": choice, "clocks": clk.summary()}), flush=True)
         del q, k, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
 
@@ -361,6 +373,10 @@ def main():
     atomic = results.get("atomic")
     for s, r in list(results.items()) + list(two_chains.items()) + list(fill.items()):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
+    choice = None
+    if atomic and "serial" in results:
+        choice = runtime_choice(dash, w, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                atomic["main_ms"], results["serial"]["main_ms"], best)
 
     # end to end through the host-buffer entry point: H2D inputs, backward, D2H gradients
     pin = [t.pin_memory() for t in host] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]
@@ -413,6 +429,7 @@ def main():
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
             "extension_two_dq_chains": two_chains or None,
             "extension_fill": fill or None,
+            "runtime_choice": choice,
             "gpu_launches": launches,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -63,6 +63,7 @@ _SIGS = {
     "dash_build_shift_fill": ([_I] * 7 + [_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                                           ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
+    "dash_fit_costs": ([_I] * 4 + [ctypes.c_double] * 2 + [ctypes.POINTER(_I)] * 2, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_sync_status": ([_P], _I),
     "dash_release_workspace": ([], None),
@@ -224,6 +225,14 @@ def dash_build_shift_fill(BH: int, n: int, causal: bool, schedule, max_ctas: int
                                        ctypes.byref(P), ctypes.byref(hs), ctypes.byref(fm), ctypes.byref(ms)))
     fill = next(k for k, v in SCHEDULES.items() if v == fm.value) if fm.value >= 0 else None
     return tasks[:nt], off[:P.value + 1], int(P.value), int(hs.value), fill, int(ms.value)
+
+
+def dash_fit_costs(BH: int, n: int, causal: bool, max_ctas: int, atomic_ms: float, serial_ms: float):
+    """Host-only.  Returns (cost_c, cost_r) fitted to the measured atomic and serial times."""
+    c, r = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().dash_fit_costs(BH, n, int(causal), max_ctas, float(atomic_ms), float(serial_ms), ctypes.byref(c),
+                                ctypes.byref(r)))
+    return int(c.value), int(r.value)
 
 
 def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):

@@ -565,6 +565,14 @@ int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int ma
   return dash::choose_ctas(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r);
 }
 
+dash_status_t dash_fit_costs(int BH, int n, int causal, int max_ctas, double atomic_ms, double serial_ms,
+                             int *cost_c_out, int *cost_r_out) {
+  if (!cost_c_out || !cost_r_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
+  std::string why = dash::fit_costs(BH, n, causal != 0, max_ctas, atomic_ms, serial_ms, cost_c_out, cost_r_out);
+  if (!why.empty()) return fail(DASH_ERR_INVALID_ARG, "dash_fit_costs: %s", why.c_str());
+  return DASH_OK;
+}
+
 int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
                          long long *makespan_out) {
   int P = 0;

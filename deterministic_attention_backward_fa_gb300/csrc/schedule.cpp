@@ -32,6 +32,7 @@
 #include "schedule.h"
 
 #include <algorithm>
+#include <cmath>
 #include <functional>
 #include <queue>
 #include <utility>
@@ -364,6 +365,29 @@ std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, i
   out->makespan = best_ms;
   if (shift_heads) *shift_heads = best_hs;
   if (fill_mode) *fill_mode = best_fm;
+  return "";
+}
+
+std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, double serial_ms, int *c, int *r) {
+  if (BH < 1 || n < 1 || P_max < 1) return "BH, n and P must be >= 1";
+  if (!(atomic_ms > 0) || !(serial_ms > 0)) return "the measured times must be positive";
+  const int P = (int)std::min<long long>(P_max, (long long)BH * n);
+  const HeadPlan ha = head_plan(kAtomic, n, causal), hs = head_plan(kSerial, n, causal);
+  const std::vector<int> pa = head_pred(ha, n), ps = head_pred(hs, n);
+  const double want = serial_ms / atomic_ms;
+  double best_err = -1;
+  for (int rr : kFitCostR) {
+    const SimResult a = simulate(ha, pa, BH, P, kFitCostC, rr, false);
+    const SimResult s = simulate(hs, ps, BH, P, kFitCostC, rr, true);
+    if (a.deadlock || s.deadlock || a.makespan <= 0) continue;
+    const double err = std::fabs((double)s.makespan / (double)a.makespan - want);
+    if (best_err < 0 || err < best_err) {
+      best_err = err;
+      *r = rr;
+    }
+  }
+  if (best_err < 0) return "schedule simulation deadlocked";
+  *c = kFitCostC;
   return "";
 }
 

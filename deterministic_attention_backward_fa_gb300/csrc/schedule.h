@@ -52,6 +52,14 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, int r, Schedule *out,
                        int *shift_heads, int *fill_mode);
 
+// Task costs fitted to measured times: c is fixed at kFitCostC and r is the
+// value of kFitCostR whose simulated serial / atomic makespan ratio (both on
+// min(P_max, chains) CTAs) is nearest the measured serial_ms / atomic_ms
+// (ties to the smaller r).  Empty string on success.
+constexpr int kFitCostC = 8;
+constexpr int kFitCostR[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128};
+std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, double serial_ms, int *c, int *r);
+
 // The deterministic schedule valid for the mask whose simulated makespan,
 // each at its own choose_ctas CTA count, is smallest (ties to the lower mode
 // number); fills its CTA count and makespan.  -1 on invalid arguments.

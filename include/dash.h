@@ -225,6 +225,18 @@ int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int ma
 int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
                          long long *makespan_out);
 
+/* Task costs for dash_choose_schedule from measured times (the pages' DAG
+ * model has a compute cost c and a reduce cost r per task; DASH overview
+ * (zskr.cn), section 2.2).  Given the measured backward (or main-kernel)
+ * times of the atomic and serial schedules for this problem, atomic_ms and
+ * serial_ms, writes c = 8 and the r in {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48,
+ * 64, 96, 128} whose simulated serial / atomic makespan ratio, both on
+ * min(max_ctas, chains) CTAs, is nearest the measured ratio (ties to the
+ * smaller r).  DASH_ERR_INVALID_ARG for sizes below 1 or times that are not
+ * positive.  Host only. */
+dash_status_t dash_fit_costs(int BH, int n, int causal, int max_ctas, double atomic_ms, double serial_ms,
+                             int *cost_c_out, int *cost_r_out);
+
 /* Synchronises `stream` and returns the device status of the calling
  * thread's current device workspace for that stream: DASH_OK, or
  * DASH_ERR_TIMEOUT if a bounded wait ran out since the last call (the word is

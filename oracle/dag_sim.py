@@ -341,6 +341,26 @@ def fill_tables(mode: str, BH: int, n: int, causal: bool, P_max: int, c: int = 4
     return tasks, off, ms, hs, fm
 
 
+FIT_COST_C = 8
+FIT_COST_R = (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128)
+
+
+def fit_costs(BH: int, n: int, causal: bool, P_max: int, atomic_ms: float, serial_ms: float):
+    """Task costs from measured times: c = FIT_COST_C and the r of FIT_COST_R
+    whose simulated serial / atomic makespan ratio (both on min(P_max, chains)
+    SMs) is nearest serial_ms / atomic_ms, ties to the smaller r."""
+    P = min(P_max, BH * n)
+    want = serial_ms / atomic_ms
+    best = None
+    for r in FIT_COST_R:
+        a = simulate(all_chains("atomic", BH, n, causal), P, FIT_COST_C, r, ordered=False).makespan
+        s = simulate(all_chains("serial", BH, n, causal), P, FIT_COST_C, r).makespan
+        err = abs(s / a - want)
+        if best is None or err < best[0]:
+            best = (err, r)
+    return FIT_COST_C, best[1]
+
+
 # Closed forms of DASH overview (zskr.cn) section 3, for m heads on n SMs.
 def t_causal_serial(m, n, c, r):
     return m * n * (c + r) + (n - 1) * r

@@ -166,6 +166,26 @@ def test_fill_rejections():
     assert "shift_fill" in dash.dash_last_error()
 
 
+@pytest.mark.parametrize("BH,n,causal,P", [(8, 4, False, 10), (6, 8, True, 12), (4, 6, True, 40), (12, 16, False, 152)])
+def test_cost_fit_recovers_simulated_costs(BH, n, causal, P):
+    # fed the simulator's own makespans as "measured" times, the fit returns
+    # the r that produced them, and the C++ fit equals the oracle's
+    for r0 in (1, 3, 8, 24, 64):
+        a = d.simulate(d.all_chains("atomic", BH, n, causal), min(P, BH * n), 8, r0, ordered=False).makespan
+        s = d.simulate(d.all_chains("serial", BH, n, causal), min(P, BH * n), 8, r0).makespan
+        assert dash.dash_fit_costs(BH, n, causal, P, 0.01 * a, 0.01 * s) == (8, r0)
+        assert d.fit_costs(BH, n, causal, P, 0.01 * a, 0.01 * s) == (8, r0)
+    for ta, ts in ((1.0, 1.0), (1.0, 1.7), (2.0, 9.0), (1.0, 0.5)):
+        assert dash.dash_fit_costs(BH, n, causal, P, ta, ts) == d.fit_costs(BH, n, causal, P, ta, ts)
+
+
+def test_cost_fit_rejects_bad_arguments():
+    for args in ((0, 4, False, 10, 1.0, 1.0), (4, 4, False, 10, 0.0, 1.0), (4, 4, False, 10, 1.0, float("nan"))):
+        with pytest.raises(dash.DashError) as ei:
+            dash.dash_fit_costs(*args)
+        assert ei.value.code == 1
+
+
 def test_schedule_choice_rejects_bad_arguments():
     with pytest.raises(dash.DashError):
         dash.dash_choose_schedule(0, 4, False, 40)
