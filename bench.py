@@ -218,6 +218,17 @@ def run_reference(args, rank, world):
     return 0
 
 
+def best_with_extensions(results, two_chains, fill, best, world, peak):
+    """The fastest deterministic layout including the two extensions (never in `value`)."""
+    cands = {best: results[best]}
+    cands.update({f"{s}+fill": r for s, r in fill.items()})
+    cands.update({f"{s}+two_dq_chains": r for s, r in two_chains.items()})
+    name = max(cands, key=lambda s: cands[s]["tflops"])
+    r = cands[name]
+    return {"schedule": name, "tflops": r["tflops"], "ratio_vs_atomic": r.get("vs_atomic"),
+            "pct_bf16_peak": 100.0 * r["tflops"] / world / peak}
+
+
 def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best):
     """The library's runtime schedule choice with task costs fitted to this run's atomic and
     serial times, against the schedule measured best."""
@@ -420,6 +431,7 @@ def main():
                        "flops_per_step": flops},
             "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
             "ratio_vs_atomic": results[best]["vs_atomic"],
+            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak),
             "schedules": results,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
