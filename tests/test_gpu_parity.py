@@ -90,6 +90,30 @@ def test_two_dq_chains_match_oracle(B, H, S, D, causal, tile):
             assert_close(f"{sched} two chains {name}", x, r)
 
 
+@pytest.mark.parametrize("S,causal,sched,H,ctas", [(256, False, "shift", 5, 10), (512, True, "symmetric_shift", 5, 10),
+                                                   (300, False, "shift", 7, 12), (640, True, "symmetric_shift", 7, 12)])
+def test_fill_small_matches_oracle(S, causal, sched, H, ctas):
+    # fill (an extension) on a small CTA budget, so that some heads run on the
+    # leftover CTAs: every head against the oracle, including a ragged tail
+    tile, D = 64, 64
+    n = (S + tile - 1) // tile
+    _, _, used, hs, fill_sched, _ = dash.dash_build_shift_fill(H, n, causal, sched, ctas)
+    assert hs < H and fill_sched is not None and used == ctas
+    P = Problem(1, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    q, k, v, do = P.f64
+    ref = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, num_ctas=ctas,
+                        shift_fill=1)
+    dash.dash_sync_status()
+    for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert_close(f"{sched} with fill {name}", x, r)
+    again = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, num_ctas=ctas,
+                          shift_fill=1)
+    dash.dash_sync_status()
+    assert all(torch.equal(a, b) for a, b in zip(got, again))
+
+
 @pytest.mark.parametrize("chains", [1, 2])
 @pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
 def test_fill_heads_equal_their_own_schedules(wname, sched, chains):
