@@ -38,6 +38,9 @@ Pins (tests/test_dag_sim.py): the four closed forms of overview section 3
 at P = n, the cyclic visiting order printed in overview section 3.2
 (tests/golden/shift_order_n4.txt), Lemma 1's consequence that the
 conflict-free schedules never wait at P = n, and coverage of every tile.
+fill_tables (an extension) is pinned by coverage, by each head's ranks
+equalling its own schedule's, and by brute force over every split of the
+heads; fit_costs by recovering the r that produced simulated makespans.
 """
 from __future__ import annotations
 
