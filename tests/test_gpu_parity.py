@@ -12,6 +12,7 @@ import torch
 import deterministic_attention_backward_fa_gb300 as dash
 import workloads
 from oracle import attention as A
+from oracle import dag_sim as d
 
 from _gpu import LSE_ABS_TOL, Problem, assert_close, err
 
@@ -145,6 +146,55 @@ def test_fill_heads_equal_their_own_schedules(wname, sched, chains):
     ref = A.backward_rows(q[b_, h_], k[b_, h_], v[b_, h_], oh, do[b_, h_], lh, w.causal, P.scale, rows)
     for name, x, r in zip(("dQ", "dK", "dV"), fill[:3], ref):
         assert_close(f"{sched} with fill {name}[{b_},{h_}] rows", x[BH - 1][rows], r)
+
+
+def _red_add_f32(acc, x):
+    """fp32 add as red.global.add.f32 performs it: round to nearest even, with
+    subnormal inputs and results flushed to (signed) zero."""
+    tiny = np.float32(np.finfo(np.float32).tiny)
+    flush = lambda a: np.where(np.abs(a) < tiny, np.copysign(np.float32(0), a), a).astype(np.float32)
+    return flush(flush(acc) + flush(x))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kernel_adds_partials_in_table_rank_order(causal):
+    # The order check: each task's fp32 dQ partial is taken from a run whose
+    # table holds that task alone (rank 0 stores its partial unchanged); the
+    # CPU then adds the partials of every tile in the schedule's rank order in
+    # fp32 (for two chains: even and odd ranks apart, then chain 0 + chain 1),
+    # and the result must equal the accumulator of the whole run bit for bit.
+    B, H, S, D, tile = 1, 2, 256, 64, 64
+    n, BH = S // tile, B * H
+    P = Problem(B, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    tiles = [(kv, q) for kv in range(n) for q in range(n) if not causal or q >= kv]
+    part = {}
+    for bh in range(BH):
+        for kv, q in tiles:
+            one = np.array([[bh, kv, q, dash.TASK_FIRST | dash.TASK_LAST]], dtype=np.int32)
+            acc = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, "serial", tile=tile, dq_accum=True,
+                                tasks=one, cta_off=np.array([0, 1], dtype=np.int32))[3]
+            dash.dash_sync_status()
+            part[(bh, kv, q)] = acc.reshape(BH, S, D)[bh, q * tile:(q + 1) * tile].cpu().numpy()
+    for sched in ("serial", "descending_q", "symmetric_shift" if causal else "shift"):
+        chains_ = d.head_chains(sched, n, causal)
+        rank = {t: rk for ch, rks in zip(chains_, d.head_ranks(sched, n, causal, chains_)) for t, rk in zip(ch, rks)}
+        for nch in (1, 2):
+            got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, dq_accum=True,
+                                dq_chains=nch)[3]
+            dash.dash_sync_status()
+            got = got.reshape(BH, S, D).cpu().numpy()
+            for bh in range(BH):
+                for q in range(n):
+                    order = sorted((rank[(kv, q)], kv) for kv, qq in tiles if qq == q)
+                    sums = [None, None]
+                    for rk, kv in order:
+                        c = rk % nch
+                        x = part[(bh, kv, q)]
+                        sums[c] = x.copy() if sums[c] is None else _red_add_f32(sums[c], x)
+                    want = sums[0] if nch == 1 or sums[1] is None else (sums[0] + sums[1]).astype(np.float32)
+                    assert np.array_equal(got[bh, q * tile:(q + 1) * tile], want), \
+                        f"{sched}, {nch} chain(s): head {bh}, dQ tile {q} differs from the rank-order sum"
 
 
 LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
