@@ -44,7 +44,7 @@ class BwdOptions(ctypes.Structure):
                 ("cost_r", ctypes.c_int), ("spin_limit_ns", ctypes.c_longlong),
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
-                ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int)]
+                ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int)]
 
 
 _LIB = None
@@ -63,6 +63,7 @@ _SIGS = {
     "dash_build_shift_fill": ([_I] * 7 + [_P, _P, ctypes.POINTER(_I), ctypes.POINTER(_I), ctypes.POINTER(_I),
                                           ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
+    "dash_check_table": ([_I] * 4 + [_P, _P, _I], _I),
     "dash_fit_costs": ([_I] * 4 + [ctypes.c_double] * 2 + [ctypes.POINTER(_I)] * 2, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_sync_status": ([_P], _I),
@@ -143,7 +144,7 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
-                     cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0):
+                     cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
     tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
@@ -152,7 +153,7 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
-                     shift_fill)
+                     shift_fill, trust_table)
     if main_events is not None:
         opt.main_begin_event = main_events[0].cuda_event
         opt.main_end_event = main_events[1].cuda_event
@@ -225,6 +226,14 @@ def dash_build_shift_fill(BH: int, n: int, causal: bool, schedule, max_ctas: int
                                        ctypes.byref(P), ctypes.byref(hs), ctypes.byref(fm), ctypes.byref(ms)))
     fill = next(k for k, v in SCHEDULES.items() if v == fm.value) if fm.value >= 0 else None
     return tasks[:nt], off[:P.value + 1], int(P.value), int(hs.value), fill, int(ms.value)
+
+
+def dash_check_table(BH: int, n: int, causal: bool, tasks, cta_off, dq_chains: int = 0):
+    """Host-only.  Raises DashError (code 6) if the table's dQ orders could not finish."""
+    t = np.ascontiguousarray(tasks, dtype=np.int32).reshape(-1, 4)
+    o = np.ascontiguousarray(cta_off, dtype=np.int32)
+    _check(lib().dash_check_table(BH, n, int(causal), dq_chains, t.ctypes.data_as(ctypes.c_void_p),
+                                  o.ctypes.data_as(ctypes.c_void_p), len(o) - 1))
 
 
 def dash_fit_costs(BH: int, n: int, causal: bool, max_ctas: int, atomic_ms: float, serial_ms: float):

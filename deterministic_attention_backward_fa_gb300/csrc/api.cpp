@@ -259,6 +259,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
     if (P > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", P, sms);
     st = validate_table(opt->tasks, opt->cta_off, P, BH, n, causal != 0);
     if (st != DASH_OK) return st;
+    if (mode != DASH_SCHED_ATOMIC && !opt->trust_table) {  // the ordered adds must be able to finish
+      why = dash::check_table_order(opt->tasks, opt->cta_off, P, BH, n, chains);
+      if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+    }
     const size_t nt = (size_t)opt->cta_off[P];
     if ((e = custom_holder.tasks.reserve(std::max<size_t>(nt, 1) * 16)) != cudaSuccess ||
         (e = custom_holder.cta_off.reserve((P + 1) * 4)) != cudaSuccess)
@@ -537,6 +541,18 @@ dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t sch
   std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
   std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
   if (makespan_out) *makespan_out = s.makespan;
+  return DASH_OK;
+}
+
+dash_status_t dash_check_table(int BH, int n, int causal, int dq_chains, const int32_t *tasks, const int32_t *cta_off,
+                               int num_ctas) {
+  if (!tasks || !cta_off || num_ctas < 1 || BH < 1 || n < 1)
+    return fail(DASH_ERR_INVALID_ARG, "dash_check_table: null table or sizes below 1");
+  if (dq_chains < 0 || dq_chains > 2) return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
+  dash_status_t st = validate_table(tasks, cta_off, num_ctas, BH, n, causal != 0);
+  if (st != DASH_OK) return st;
+  const std::string why = dash::check_table_order(tasks, cta_off, num_ctas, BH, n, dq_chains == 2 ? 2 : 1);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
   return DASH_OK;
 }
 

@@ -32,6 +32,7 @@
 #include "schedule.h"
 
 #include <algorithm>
+#include <string>
 #include <cmath>
 #include <functional>
 #include <queue>
@@ -365,6 +366,71 @@ std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, i
   out->makespan = best_ms;
   if (shift_heads) *shift_heads = best_hs;
   if (fill_mode) *fill_mode = best_fm;
+  return "";
+}
+
+std::string check_table_order(const int32_t *tasks, const int32_t *cta_off, int P, int BH, int n, int chains) {
+  if (chains != 1 && chains != 2) return "chains must be 1 or 2";
+  const size_t keys = (size_t)BH * n * chains;  // (head, dQ tile, chain)
+  // every chain of every tile holds positions 0 .. count-1 exactly once
+  std::vector<int> count(keys, 0), seen_max(keys, -1);
+  std::vector<std::vector<char>> seen(keys);
+  const int total = cta_off[P];
+  for (int t = 0; t < total; ++t) {
+    const int32_t *k = tasks + 4 * (size_t)t;
+    const int rank = k[3] & kRankMask;
+    const size_t key = ((size_t)k[0] * n + k[2]) * chains + rank % chains;
+    const int pos = rank / chains;
+    std::vector<char> &sv = seen[key];
+    if ((int)sv.size() <= pos) sv.resize(pos + 1, 0);
+    if (sv[pos]) return "task " + std::to_string(t) + " repeats a rank of its dQ tile";
+    sv[pos] = 1;
+    ++count[key];
+    seen_max[key] = std::max(seen_max[key], pos);
+  }
+  for (size_t key = 0; key < keys; ++key)
+    if (seen_max[key] + 1 != count[key]) return "a dQ tile's ranks have a gap: a reduction would wait forever";
+  // run the table: a CTA's adds go in table order, each waiting for the
+  // previous position of its chain; a CTA blocked on a position is resumed
+  // when that position's predecessor is done
+  std::vector<int> next(keys, 0), ptr(cta_off, cta_off + P);
+  std::vector<int> waiter(total, -1);  // CTA blocked on the task that holds (key, pos); indexed by that task
+  std::vector<int> holder;             // task index of (key, pos), built below
+  std::vector<size_t> base(keys + 1, 0);
+  for (size_t key = 0; key < keys; ++key) base[key + 1] = base[key] + count[key];
+  holder.assign(base[keys], -1);
+  for (int t = 0; t < total; ++t) {
+    const int32_t *k = tasks + 4 * (size_t)t;
+    const int rank = k[3] & kRankMask;
+    const size_t key = ((size_t)k[0] * n + k[2]) * chains + rank % chains;
+    holder[base[key] + rank / chains] = t;
+  }
+  std::vector<int> ready;
+  for (int s = 0; s < P; ++s) ready.push_back(s);
+  int finished = 0;
+  while (!ready.empty()) {
+    const int s = ready.back();
+    ready.pop_back();
+    while (ptr[s] < cta_off[s + 1]) {
+      const int t = ptr[s];
+      const int32_t *k = tasks + 4 * (size_t)t;
+      const int rank = k[3] & kRankMask;
+      const size_t key = ((size_t)k[0] * n + k[2]) * chains + rank % chains;
+      const int pos = rank / chains;
+      if (pos != next[key]) {  // blocked until the predecessor's add is done
+        waiter[holder[base[key] + pos - 1]] = s;
+        break;
+      }
+      ++next[key];
+      ++ptr[s];
+      if (waiter[t] >= 0) {  // a CTA waited for this add
+        ready.push_back(waiter[t]);
+        waiter[t] = -1;
+      }
+    }
+    if (ptr[s] == cta_off[s + 1]) ++finished;
+  }
+  if (finished != P) return "the table's dQ orders wait on one another in a cycle: it would never finish";
   return "";
 }
 

@@ -52,6 +52,16 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
 std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, int r, Schedule *out,
                        int *shift_heads, int *fill_mode);
 
+// Checks that a task table (4 int32 per task, cta_off of P + 1 entries) runs
+// to completion when each CTA performs its tasks' dQ adds in table order and a
+// task's add waits for its predecessor in the tile's order: with `chains`
+// chains (1 or 2), the task of rank k is position k / chains of chain
+// k % chains.  Every tile's positions in each chain must be 0, 1, ... with no
+// gap or repeat, and an event-driven run of the table must reach every CTA's
+// end (no cycle of waits).  Bounds and run structure are checked elsewhere.
+// Empty string when the table is sound, else the reason.
+std::string check_table_order(const int32_t *tasks, const int32_t *cta_off, int P, int BH, int n, int chains);
+
 // Task costs fitted to measured times: c is fixed at kFitCostC and r is the
 // value of kFitCostR whose simulated serial / atomic makespan ratio (both on
 // min(P_max, chains) CTAs) is nearest the measured serial_ms / atomic_ms

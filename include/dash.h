@@ -118,12 +118,18 @@ typedef struct {
                             * Each head keeps its own schedule's dQ order, so the result is deterministic;
                             * the filled heads' bits are the fill schedule's.  num_ctas, if set, is the CTA
                             * budget. */
+  int trust_table;         /* with tasks: 0 = check the table's dQ orders on the host before the launch
+                            * (dash_check_table; DASH_ERR_SCHEDULE if they could not finish); 1 = bounds
+                            * checks only, so that an inconsistent table reaches the device, whose bounded
+                            * waits then report DASH_ERR_TIMEOUT (testing). */
 } dash_bwd_options_t;
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
- * bounds-checked on the host (DASH_ERR_SCHEDULE if an index is out of range);
- * ranks are taken as given, so an inconsistent table makes the device waits
- * run out, which dash_sync_status() then reports as DASH_ERR_TIMEOUT. */
+ * checked on the host before the launch: indices in range, runs on one KV tile
+ * each, and (for an ordered schedule, unless trust_table is set) dQ orders
+ * that can finish, as dash_check_table states; DASH_ERR_SCHEDULE otherwise.
+ * With trust_table set, an inconsistent table makes the device waits run out,
+ * which dash_sync_status() then reports as DASH_ERR_TIMEOUT. */
 dash_status_t dash_attn_bwd_ex(const void *q, const void *k, const void *v, const void *o,
                                const void *dout, const float *lse,
                                void *dq, void *dk, void *dv,
@@ -183,6 +189,18 @@ long long dash_schedule_num_tasks(int BH, int n, int causal, dash_schedule_t sch
 dash_status_t dash_build_schedule(int BH, int n, int causal, dash_schedule_t schedule, int P,
                                   int cost_c, int cost_r, int32_t *tasks_out,
                                   int32_t *cta_off_out, long long *makespan_out);
+
+/* Checks a task table for an ordered schedule on the host (the pages' DAG:
+ * a dQ tile's reductions run in rank order, DASH overview (zskr.cn),
+ * section 2.2).  tasks holds 4 int32 per task in the encoding above and
+ * cta_off num_ctas + 1 offsets.  Besides indices and runs, every dQ tile's
+ * ranks must be 0, 1, ... without gap or repeat (with dq_chains = 2, in each
+ * parity apart), and the table must finish when each CTA performs its adds in
+ * table order, each waiting for its predecessor in the tile's order (no cycle
+ * of waits).  DASH_OK, DASH_ERR_SCHEDULE with the reason in
+ * dash_last_error(), or DASH_ERR_INVALID_ARG.  Host only. */
+dash_status_t dash_check_table(int BH, int n, int causal, int dq_chains, const int32_t *tasks, const int32_t *cta_off,
+                               int num_ctas);
 
 /* Fill, an extension beyond the pages' schedules, for DASH_SCHED_SHIFT (full
  * mask) and DASH_SCHED_SYMMETRIC_SHIFT (causal).  Each of their chains waits

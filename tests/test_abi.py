@@ -186,6 +186,83 @@ def test_cost_fit_rejects_bad_arguments():
         assert ei.value.code == 1
 
 
+def _finishes(tasks, off, chains):
+    """Plain reference for the table check: repeat passes over the CTAs, letting each
+    perform its next add when the previous position of its chain is done."""
+    nxt, ptr = {}, list(off[:-1])
+    moved = True
+    while moved:
+        moved = False
+        for s in range(len(off) - 1):
+            while ptr[s] < off[s + 1]:
+                bh, kv, q, w = (int(x) for x in tasks[ptr[s]])
+                rank = w & dash.TASK_RANK_MASK
+                key = (bh, q, rank % chains)
+                if nxt.get(key, 0) != rank // chains:
+                    break
+                nxt[key] = rank // chains + 1
+                ptr[s] += 1
+                moved = True
+    return all(ptr[s] == off[s + 1] for s in range(len(off) - 1))
+
+
+def test_table_check_accepts_generated_tables():
+    for mode, causal, n in (("serial", False, 4), ("descending_q", True, 5), ("shift", False, 4),
+                            ("symmetric_shift", True, 6)):
+        for P in (3, 8, 40):
+            try:
+                t, off, _ = dash.dash_build_schedule(3, n, causal, mode, P)
+            except dash.DashError:
+                continue
+            for chains in (0, 2):
+                dash.dash_check_table(3, n, causal, t, off, chains)
+
+
+def test_table_check_rejects_gaps_repeats_and_cycles():
+    F, L = dash.TASK_FIRST, dash.TASK_LAST
+    bad = {
+        # KV 0 adds to Q tile 0 at rank 1 before Q tile 1 at rank 0; KV 1 the other way round
+        "cycle": ([[0, 0, 0, 1 | F], [0, 0, 1, 0 | L], [0, 1, 1, 1 | F], [0, 1, 0, 0 | L]], [0, 2, 4], 2),
+        "gap": ([[0, 0, 0, 0 | F | L], [0, 2, 0, 2 | F | L]], [0, 1, 2], 3),
+        "repeats": ([[0, 0, 0, 0 | F | L], [0, 1, 0, 0 | F | L]], [0, 1, 2], 2),
+    }
+    for word, (t, off, n) in bad.items():
+        with pytest.raises(dash.DashError) as ei:
+            dash.dash_check_table(1, n, False, np.array(t, dtype=np.int32), off)
+        assert ei.value.code == 6 and word in dash.dash_last_error(), dash.dash_last_error()
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_table_check_agrees_with_a_plain_run(seed):
+    # random tables: each CTA runs one KV tile over the Q tiles in a random
+    # order; each dQ tile's ranks are a random permutation of its KV tiles
+    rng = np.random.default_rng(seed)
+    verdicts = set()
+    for _ in range(150):
+        n, BH = int(rng.integers(2, 5)), int(rng.integers(1, 3))
+        chains = int(rng.integers(1, 3))
+        ranks = {(bh, q): rng.permutation(n) for bh in range(BH) for q in range(n)}
+        tasks, off = [], [0]
+        for bh in range(BH):
+            for kv in range(n):
+                order = rng.permutation(n)
+                for j, q in enumerate(order):
+                    w = int(ranks[(bh, q)][kv]) | (dash.TASK_FIRST if j == 0 else 0) | \
+                        (dash.TASK_LAST if j == n - 1 else 0)
+                    tasks.append([bh, kv, int(q), w])
+                off.append(len(tasks))
+        tasks = np.array(tasks, dtype=np.int32)
+        ok = _finishes(tasks, off, chains)
+        verdicts.add(ok)
+        if ok:
+            dash.dash_check_table(BH, n, False, tasks, off, chains)
+        else:
+            with pytest.raises(dash.DashError) as ei:
+                dash.dash_check_table(BH, n, False, tasks, off, chains)
+            assert ei.value.code == 6
+    assert verdicts == {True, False}
+
+
 def test_schedule_choice_rejects_bad_arguments():
     with pytest.raises(dash.DashError):
         dash.dash_choose_schedule(0, 4, False, 40)

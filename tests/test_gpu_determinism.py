@@ -103,8 +103,14 @@ def test_stuck_semaphore_times_out_and_context_survives():
     i = int(np.nonzero((tasks[:, 3] & dash.TASK_RANK_MASK) == 1)[0][0])
     tasks[i, 3] = (tasks[i, 3] & ~dash.TASK_RANK_MASK) | 2
     dq, dk, dv = (torch.empty_like(P.q) for _ in range(3))
+    # the host check refuses such a table before the launch ...
+    with pytest.raises(dash.DashError) as ei:
+        dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, dq, dk, dv, False, P.scale, "serial",
+                              tasks=tasks, cta_off=off, spin_limit_ns=50_000_000)
+    assert ei.value.code == 6, str(ei.value)
+    # ... and, told to trust it, the device's bounded waits run out and say so
     dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, dq, dk, dv, False, P.scale, "serial",
-                          tasks=tasks, cta_off=off, spin_limit_ns=50_000_000)
+                          tasks=tasks, cta_off=off, spin_limit_ns=50_000_000, trust_table=1)
     with pytest.raises(dash.DashError) as ei:
         dash.dash_sync_status()
     assert ei.value.code == 4, str(ei.value)
