@@ -111,8 +111,9 @@ typedef struct {
                             * semaphore, and dQ = chain 0 + chain 1.  Deterministic, with a different
                             * summation order from 1.  With num_ctas = 0, shift then takes every SM
                             * instead of whole gangs.  Ignored by the atomic schedule. */
-  int shift_fill;          /* DASH_SCHED_SHIFT and DASH_SCHED_SYMMETRIC_SHIFT (with one or two chains): 0 = the pages'
-                            * schedule; 1 = with fill (an extension beyond the pages): whole gangs of CTAs run
+  int shift_fill;          /* DASH_SCHED_SHIFT and DASH_SCHED_SYMMETRIC_SHIFT, with one or two chains:
+                            * 0 = the pages' schedule; 1 = with fill (an extension beyond the pages): whole
+                            * gangs of CTAs run
                             * the schedule for most heads, and the CTAs they leave idle run the other heads
                             * with a fill schedule (serial or descending_q), as dash_build_shift_fill lays out.
                             * Each head keeps its own schedule's dQ order, so the result is deterministic;
