@@ -1,0 +1,37 @@
+"""Host-side helpers of bench.py (no GPU): the fastest deterministic layout
+including the extensions, and the runtime schedule choice with fitted costs."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import deterministic_attention_backward_fa_gb300 as dash  # noqa: E402
+import workloads  # noqa: E402
+
+
+def test_best_with_extensions_picks_the_fastest_layout():
+    res = {"atomic": {"tflops": 900.0, "vs_atomic": 1.0}, "serial": {"tflops": 600.0, "vs_atomic": 0.667},
+           "shift": {"tflops": 750.0, "vs_atomic": 0.833}}
+    two = {"shift": {"tflops": 800.0, "vs_atomic": 0.889}}
+    fill = {"shift": {"tflops": 850.0, "vs_atomic": 0.944}}
+    b = bench.best_with_extensions(res, two, fill, "shift", 1, 2000.0)
+    assert b["schedule"] == "shift+fill" and b["tflops"] == 850.0 and abs(b["pct_bf16_peak"] - 42.5) < 1e-9
+    b = bench.best_with_extensions(res, two, {}, "shift", 1, 2000.0)
+    assert b["schedule"] == "shift+two_dq_chains"
+    b = bench.best_with_extensions(res, {}, {}, "shift", 2, 2000.0)   # whole-job value over two GPUs
+    assert b["schedule"] == "shift" and abs(b["pct_bf16_peak"] - 18.75) < 1e-9
+
+
+def test_runtime_choice_uses_the_fitted_costs():
+    import __graft_entry__
+    __graft_entry__.build()
+    w = workloads.WORKLOADS["full_s4096_d128"]
+    BH, n = w.B * w.H, w.S // w.tile
+    ch = bench.runtime_choice(dash, w, 152, 1.0, 1.45, "shift")
+    c, r = dash.dash_fit_costs(BH, n, w.causal, 152, 1.0, 1.45)
+    assert (ch["cost_c"], ch["cost_r"]) == (c, r)
+    name, ctas, _ = dash.dash_choose_schedule(BH, n, w.causal, 152, c, r)
+    assert (ch["chosen"], ch["ctas"]) == (name, ctas)
+    assert ch["agrees"] == (name == "shift")
