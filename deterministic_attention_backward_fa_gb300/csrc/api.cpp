@@ -235,9 +235,11 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const int c = (opt && opt->cost_c > 0) ? opt->cost_c : 4;
   const int r = (opt && opt->cost_r > 0) ? opt->cost_r : 1;
   const long long spin = (opt && opt->spin_limit_ns > 0) ? opt->spin_limit_ns : kDefaultSpinNs;
-  if (opt && (opt->dq_chains < 0 || opt->dq_chains > 2)) return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
+  if (opt && (opt->dq_chains < 0 || opt->dq_chains > 2))
+    return fail(DASH_ERR_INVALID_ARG, "dq_chains must be 0, 1 or 2");
   const int chains = (mode != DASH_SCHED_ATOMIC && opt && opt->dq_chains == 2) ? 2 : 1;
-  if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1)) return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
+  if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1))
+    return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
   const bool fill = (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT) && opt && opt->shift_fill == 1;
 
   int dev = 0;
@@ -287,7 +289,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       // With fill, the SMs that whole gangs leave idle run other heads in the
       // serial order (num_ctas, if given, is the CTA budget).
       int Puse = want;
-      if (!Puse && !fill && chains == 2 && mode == DASH_SCHED_SHIFT) Puse = (int)std::min<long long>(sms, (long long)BH * n);
+      if (!Puse && !fill && chains == 2 && mode == DASH_SCHED_SHIFT)
+        Puse = (int)std::min<long long>(sms, (long long)BH * n);
       if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
       if (Puse < 1 && !fill) {
         g_sched.erase(key);
