@@ -14,14 +14,21 @@
 // statistics, the fp32 dQ accumulator and the schedule table.  Problems whose
 // scratch would exceed kScratchBytes are rejected.  Every call shares the
 // array and leaves its contents behind; the parts that must start at zero
-// (status word, semaphores, accumulator) are cleared by each call.  Two calls
+// (the status word, the semaphores and, for the atomic schedule, the
+// accumulator) are cleared by each call.  Two calls
 // whose GPU work overlaps (different streams, or different host threads) race
 // on the array; calls on one stream are ordered and safe.
 //
-// The kernels are the same ones dash_attn_bwd launches; only where their
-// scratch lives differs.  The call synchronises its stream before it returns,
-// so that it can report a device wait that ran out (the status word lives in
-// the shared array, which a later call would clear).
+// The kernels are the same ones dash_attn_bwd launches, with the same schedule
+// table, so a deterministic schedule gives the same bits as dash_attn_bwd;
+// only where their scratch lives differs.  The call synchronises its stream
+// before it returns, so that it can report a device wait that ran out (the
+// status word lives in the shared array, which a later call would clear).
+//
+// The array's device address is looked up once per device, by the first call
+// on that device, and kept for the life of the process.  After
+// cudaDeviceReset the library's module is loaded anew and that address is no
+// longer valid, so the entry point must not be used after a device reset.
 #include "dash.h"
 
 #include <cuda.h>
@@ -42,6 +49,8 @@
 
 namespace dash {
 void set_last_error(const char *msg);  // api.cpp
+// TMA map over a contiguous bf16 [BH][S][D] tensor, as the backward's kernels read it (api.cpp)
+bool encode_bhsd_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows);
 }
 
 namespace {
@@ -68,31 +77,6 @@ dash_status_t fail(dash_status_t code, const char *fmt, ...) {
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-bool encode_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows) {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
@@ -104,6 +88,7 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   if (D != 64 && D != 128) return fail(DASH_ERR_UNSUPPORTED, "head dim %d not supported (64 or 128)", D);
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DASH_ERR_INVALID_ARG, "scale must be finite and > 0");
   const long long BH = (long long)B * H;
+  if (BH > (1LL << 30) || S > (1 << 30)) return fail(DASH_ERR_INVALID_ARG, "problem too large");
   if (BH == 0 || S == 0) return DASH_OK;
   for (const void *p : {q, k, v, o, dout, (const void *)lse, (const void *)dq, (const void *)dk, (const void *)dv})
     if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return fail(DASH_ERR_INVALID_ARG, "null or misaligned pointer");
@@ -162,8 +147,10 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   const dash::Schedule &sch = it->second;
 
   dash::BwdMaps maps;
-  if (!encode_map(&maps.q, q, (int)BH, S, D, T) || !encode_map(&maps.dout, dout, (int)BH, S, D, T) ||
-      !encode_map(&maps.k, k, (int)BH, S, D, 128) || !encode_map(&maps.v, v, (int)BH, S, D, 128))
+  if (!dash::encode_bhsd_map(&maps.q, q, (int)BH, S, D, T) ||
+      !dash::encode_bhsd_map(&maps.dout, dout, (int)BH, S, D, T) ||
+      !dash::encode_bhsd_map(&maps.k, k, (int)BH, S, D, 128) ||
+      !dash::encode_bhsd_map(&maps.v, v, (int)BH, S, D, 128))
     return fail(DASH_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
   // the table goes into the scratch; the status word starts at zero
@@ -181,7 +168,9 @@ extern "C" dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, con
   pre.lse2 = reinterpret_cast<float *>(base + o_lse2);
   pre.delta = reinterpret_cast<float *>(base + o_delta);
   pre.dq_accum = reinterpret_cast<float *>(base + o_accum);
-  pre.accum_floats = rows * D;
+  // Ordered schedules store the partial of rank 0, so only the atomic
+  // schedule's accumulator must start at zero (as in dash_attn_bwd).
+  pre.accum_floats = mode == DASH_SCHED_ATOMIC ? rows * D : 0;
   pre.sem = reinterpret_cast<int *>(base + o_sem);
   pre.sem_count = (int)(BH * n * dash::kSemStride);
   pre.S = S;
