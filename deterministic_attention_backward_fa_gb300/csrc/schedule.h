@@ -67,7 +67,7 @@ std::string check_table_order(const int32_t *tasks, const int32_t *cta_off, int 
 // min(P_max, chains) CTAs) is nearest the measured serial_ms / atomic_ms
 // (ties to the smaller r).  Empty string on success.
 constexpr int kFitCostC = 8;
-constexpr int kFitCostR[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128};
+constexpr int kFitCostR[] = {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512};
 std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, double serial_ms, int *c, int *r);
 
 // The deterministic schedule valid for the mask whose simulated makespan,

@@ -345,7 +345,7 @@ def fill_tables(mode: str, BH: int, n: int, causal: bool, P_max: int, c: int = 4
 
 
 FIT_COST_C = 8
-FIT_COST_R = (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128)
+FIT_COST_R = (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512)
 
 
 def fit_costs(BH: int, n: int, causal: bool, P_max: int, atomic_ms: float, serial_ms: float):

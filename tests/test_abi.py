@@ -170,7 +170,7 @@ def test_fill_rejections():
 def test_cost_fit_recovers_simulated_costs(BH, n, causal, P):
     # fed the simulator's own makespans as "measured" times, the fit returns
     # the r that produced them, and the C++ fit equals the oracle's
-    for r0 in (1, 3, 8, 24, 64):
+    for r0 in (1, 3, 8, 24, 64, 256):
         a = d.simulate(d.all_chains("atomic", BH, n, causal), min(P, BH * n), 8, r0, ordered=False).makespan
         s = d.simulate(d.all_chains("serial", BH, n, causal), min(P, BH * n), 8, r0).makespan
         assert dash.dash_fit_costs(BH, n, causal, P, 0.01 * a, 0.01 * s) == (8, r0)
