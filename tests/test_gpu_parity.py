@@ -156,14 +156,22 @@ def _red_add_f32(acc, x):
     return flush(flush(acc) + flush(x))
 
 
+# (S, D, tile) of the order check: one case per kernel instantiation that the
+# workloads use (D = 64 with 64- and 128-row tiles, D = 128 with 128-row tiles;
+# the last two are the ones the large workloads run, with their stage counts
+# and, at D = 128, dQ in the dP^T columns of tensor memory)
+ORDER_CASES = [(256, 64, 64), (512, 128, 128), (512, 64, 128)]
+
+
+@pytest.mark.parametrize("S,D,tile", ORDER_CASES, ids=[f"s{s}_d{d}_t{t}" for s, d, t in ORDER_CASES])
 @pytest.mark.parametrize("causal", [False, True])
-def test_kernel_adds_partials_in_table_rank_order(causal):
+def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
     # The order check: each task's fp32 dQ partial is taken from a run whose
     # table holds that task alone (rank 0 stores its partial unchanged); the
     # CPU then adds the partials of every tile in the schedule's rank order in
     # fp32 (for two chains: even and odd ranks apart, then chain 0 + chain 1),
     # and the result must equal the accumulator of the whole run bit for bit.
-    B, H, S, D, tile = 1, 2, 256, 64, 64
+    B, H = 1, 2
     n, BH = S // tile, B * H
     P = Problem(B, H, S, D, causal)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
