@@ -95,6 +95,18 @@ struct DevBuf {
     if (e == cudaSuccess) bytes = want;
     return e;
   }
+  // Stream-ordered growth for buffers that only work on `s` uses: the old
+  // block is freed and the new one allocated in the stream's order, so the
+  // call does not synchronise the device.
+  cudaError_t reserve_on(size_t want, cudaStream_t s) {
+    if (want <= bytes) return cudaSuccess;
+    if (ptr) cudaFreeAsync(ptr, s);
+    ptr = nullptr;
+    bytes = 0;
+    cudaError_t e = cudaMallocAsync(&ptr, want, s);
+    if (e == cudaSuccess) bytes = want;
+    return e;
+  }
 };
 
 // Copy streams and events of dash_attn_bwd_host, which pipelines the host
@@ -332,9 +344,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const long long rows_padded = (long long)n * T;
   const long long total_rows = (long long)BH * rows_padded;
   const long long accum_floats = total_rows * D;
-  if ((e = w->accum.reserve(accum_floats * chains * 4)) != cudaSuccess ||
-      (e = w->lse2.reserve(total_rows * 4)) != cudaSuccess || (e = w->delta.reserve(total_rows * 4)) != cudaSuccess ||
-      (e = w->sem.reserve((size_t)BH * n * chains * dash::kSemStride * 4)) != cudaSuccess ||
+  if ((e = w->accum.reserve_on(accum_floats * chains * 4, stream)) != cudaSuccess ||
+      (e = w->lse2.reserve_on(total_rows * 4, stream)) != cudaSuccess ||
+      (e = w->delta.reserve_on(total_rows * 4, stream)) != cudaSuccess ||
+      (e = w->sem.reserve_on((size_t)BH * n * chains * dash::kSemStride * 4, stream)) != cudaSuccess ||
       (e = ensure_status(w)) != cudaSuccess)
     return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
 
@@ -408,6 +421,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
 namespace dash {
 // Lets other translation units of the library report through dash_last_error().
 void set_last_error(const char *msg) { g_last_error = msg; }
+// The backward's tensor maps for other translation units of the library.
+bool encode_bhsd_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows) {
+  return make_map(m, base, BH, S, D, box_rows) == DASH_OK;
+}
 }  // namespace dash
 
 extern "C" {

@@ -28,8 +28,10 @@
  *    dash_last_error() describes the last failure of the calling thread.
  *  - The library keeps a per-(device, stream) workspace (fp32 dQ accumulator,
  *    per-row softmax statistics, semaphores, status word) and a cache of
- *    schedule tables.  It grows them with cudaMalloc on first use of a larger
- *    shape; dash_release_workspace() frees them.  Two calls that run
+ *    schedule tables.  It grows the buffers that only the call's stream uses
+ *    with cudaMallocAsync / cudaFreeAsync on that stream on first use of a
+ *    larger shape (the status word and the tables with cudaMalloc, once);
+ *    dash_release_workspace() frees them.  Two calls that run
  *    concurrently on the same stream cannot overlap, so the workspace is never
  *    shared by concurrent kernels.
  */
@@ -158,16 +160,21 @@ dash_status_t dash_attn_bwd_host(const void *q, const void *k, const void *v, co
  * device memory, a runtime with a fixed memory budget reserved up front, or
  * code that cannot afford an allocation that may block or fail.  (The DASH
  * pages have no counterpart; this is a property of this library.)
- * Same arguments and results as dash_attn_bwd.  The workspace lives in one
- * fixed 32 MiB array of device memory inside the library, present on every
- * GPU that loads the library until the process exits; problems whose
- * workspace does not fit (roughly B*H*S*D above 7.8 M elements) return
- * DASH_ERR_UNSUPPORTED with the required size in dash_last_error().  The
- * first call on a device looks up the array's device address (make that
- * first call before any stream capture).  Every call clears what must start at
- * zero, but all calls share the array: calls whose GPU work overlaps (other
- * streams or threads) race on it.  The call synchronises `stream` before it
- * returns and reports a device wait that ran out as DASH_ERR_TIMEOUT. */
+ * Same arguments and results as dash_attn_bwd: the same kernels and the same
+ * schedule table, so a deterministic schedule returns the same bits.  The
+ * workspace lives in one fixed 32 MiB array of device memory inside the
+ * library, present on every GPU that loads the library until the process
+ * exits; problems whose workspace does not fit (roughly B*H*S*D above 7.8 M
+ * elements) return DASH_ERR_UNSUPPORTED with the required size in
+ * dash_last_error().  The first call on a device does a one-time set-up: it
+ * looks up the array's device address, which stays valid until the process
+ * exits or the device is reset (do not use this entry point after
+ * cudaDeviceReset); make that first call before any stream capture.  Every
+ * call clears what must start at zero, but all calls share the array: calls
+ * whose GPU work overlaps (other streams or threads) race on it.  The call
+ * copies the schedule table and the status word between host and device and
+ * synchronises `stream` before it returns; it reports a device wait that ran
+ * out as DASH_ERR_TIMEOUT. */
 dash_status_t dash_attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                     const void *dout, const float *lse,
                                     void *dq, void *dk, void *dv,
@@ -249,9 +256,9 @@ int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, in
  * (zskr.cn), section 2.2).  Given the measured backward (or main-kernel)
  * times of the atomic and serial schedules for this problem, atomic_ms and
  * serial_ms, writes c = 8 and the r in {1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48,
- * 64, 96, 128} whose simulated serial / atomic makespan ratio, both on
- * min(max_ctas, chains) CTAs, is nearest the measured ratio (ties to the
- * smaller r).  DASH_ERR_INVALID_ARG for sizes below 1 or times that are not
+ * 64, 96, 128, 192, 256, 384, 512} whose simulated serial / atomic makespan
+ * ratio, both on min(max_ctas, chains) CTAs, is nearest the measured ratio
+ * (ties to the smaller r).  DASH_ERR_INVALID_ARG for sizes below 1 or times that are not
  * positive.  Host only. */
 dash_status_t dash_fit_costs(int BH, int n, int causal, int max_ctas, double atomic_ms, double serial_ms,
                              int *cost_c_out, int *cost_r_out);
