@@ -11,7 +11,10 @@ reduction (dq_chains = 2, a different fixed summation order); those figures go
 to `extension_two_dq_chains` and never into `value`.  Shift and symmetric shift
 are also timed with fill (shift_fill = 1: the SMs that whole gangs of their
 chains leave idle run some heads in the serial or descending order), under
-`extension_fill`, never in `value`.
+`extension_fill`, never in `value`.  The long causal workload
+(causal_s16384_d128) is timed in the same run, every schedule of its mask and
+symmetric shift with fill, and reported under `workloads` with its own ratio
+to atomic and roofline fraction (`--also` names other workloads; '' skips it).
 
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
 
@@ -66,6 +69,9 @@ def parse():
                     help="skip timing the optional two-chain dQ reduction (dq_chains = 2)")
     ap.add_argument("--no-shift-fill", action="store_true",
                     help="skip timing shift and symmetric shift with fill (shift_fill = 1)")
+    ap.add_argument("--also", default="causal_s16384_d128",
+                    help="comma-separated further workloads timed in the same run and reported under "
+                         "`workloads` (every schedule of the mask and fill; '' for none)")
     ap.add_argument("--sweep", action="store_true",
                     help="time the pages' sweep (16384 tokens, S = 512..16384, D = 64/128, both masks) "
                          "and print one JSON line per configuration instead of the bench line")
@@ -287,6 +293,83 @@ def run_sweep(args, dash):
         torch.cuda.empty_cache()
 
 
+def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
+    """Times each (schedule, dq_chains, shift_fill) of `runs`: W warm-up steps, then K steps, each
+    bracketed by CUDA events on the launching stream, with the main kernel's own events inside."""
+    q, k, v, o, do, lse, dq, dk, dv = tensors
+    flops = w.flops()
+    results, two_chains, fill = {}, {}, {}
+    launches = 0
+    for sched, chains, shift_fill in runs:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for e in evs:
+            for x in e:
+                x.record(stream)
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                  dq_chains=chains, shift_fill=shift_fill)
+        dash.dash_sync_status()
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(1)   # evict the previous step's working set from L2
+            evs[i][0].record(stream)
+            dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                  main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
+                                  shift_fill=shift_fill)
+            evs[i][3].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        dash.dash_sync_status()
+        launches += dash.KERNELS_PER_BWD * args.steps
+        step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
+        main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
+        total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
+        (fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
+            "ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
+            "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
+    return results, two_chains, fill, launches
+
+
+def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
+    """Every schedule of the workload's mask (one dQ chain) and shift / symmetric shift with fill, timed
+    like the main line; summarised with the best of the pages' deterministic schedules, its ratio to
+    atomic and the main kernel's roofline fraction."""
+    q, k, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
+    o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
+    dash.dash_sync_status()
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+    runs = [(s, 1, 0) for s in w.schedules]
+    runs += [(s, 1, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+    results, _, fill, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
+                                           stream, world, dev, barrier)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    atomic = results["atomic"]
+    for r in list(results.values()) + list(fill.values()):
+        r["vs_atomic"] = r["tflops"] / atomic["tflops"]
+    det = {s: r for s, r in results.items() if s != "atomic"}
+    best = max(det, key=lambda s: det[s]["tflops"])
+    achieved = w.flops() / (results[best]["main_ms"] / 1e3) / 1e12
+    out = {"config": {"B": w.B, "H": w.H, "S": w.S, "D": w.D, "mask": "causal" if w.causal else "full",
+                      "tile": w.tile, "flops_per_step": w.flops()},
+           "best_deterministic": best, "tflops": results[best]["tflops"],
+           "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
+           "ratio_vs_atomic": results[best]["vs_atomic"], "schedules": results,
+           "extension_fill": fill or None,
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                        "frac": achieved / peak, "kernel": "dash_bwd_main",
+                        "peak_source": f"{peak_kind} bf16_tflops (burst)"},
+           "launches": launches}
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+    return out
+
+
+
 def main():
     args = parse()
     rank, world, local_rank = dist_env()
@@ -338,45 +421,17 @@ def main():
         except (ValueError, IndexError):
             pass
 
-    results = {}
-    two_chains = {}   # the optional two-chain dQ reduction (an extension beyond the pages' order)
-    fill = {}         # fill of the leftover SMs (an extension beyond the pages' schedules)
-    launches = 0
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
     runs = [(s, 1, 0) for s in scheds] + [(s, 2, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
     runs += [(s, 1, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
     with ClockSampler(gpu_index) as clk:
-        for sched, chains, shift_fill in runs:
-            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-                    torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(args.steps)]
-            for e in evs:
-                for x in e:
-                    x.record(stream)
-            for _ in range(args.warmup):
-                flush.fill_(1)
-                dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                      dq_chains=chains, shift_fill=shift_fill)
-            dash.dash_sync_status()
-            barrier()
-            torch.cuda.synchronize()
-            for i in range(args.steps):
-                flush.fill_(1)   # evict the previous step's working set from L2
-                evs[i][0].record(stream)
-                dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                      main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
-                                      shift_fill=shift_fill)
-                evs[i][3].record(stream)
-            torch.cuda.synchronize()
-            barrier()
-            dash.dash_sync_status()
-            launches += dash.KERNELS_PER_BWD * args.steps
-            step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
-            main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
-            total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-            (fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
-                "ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
-                "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
+        results, two_chains, fill, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args,
+                                                        flush, stream, world, dev, barrier)
+        also = {}
+        for name in [x for x in args.also.split(",") if x and x != w.name]:
+            also[name] = time_other_workload(dash, workloads.WORKLOADS[name], args, flush, stream, world, dev,
+                                             barrier)
+            launches += also[name].pop("launches")
     clocks = clk.summary()
 
     det = {s: r for s, r in results.items() if s != "atomic"} or results
@@ -439,6 +494,7 @@ def main():
             "e2e": None if not e2e_steps else {"value": world * flops * e2e_steps / e2e_s / 1e12, "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
+            "workloads": also or None,
             "extension_two_dq_chains": two_chains or None,
             "extension_fill": fill or None,
             "runtime_choice": choice,
