@@ -44,7 +44,11 @@ class BwdOptions(ctypes.Structure):
                 ("cost_r", ctypes.c_int), ("spin_limit_ns", ctypes.c_longlong),
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
-                ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int)]
+                ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int),
+                ("trace", ctypes.c_void_p)]
+
+# Slots of a trace row (dash_bwd_options_t.trace): see include/dash.h.
+TRACE_SLOTS = 17
 
 
 _LIB = None
@@ -144,12 +148,14 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
-                     cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0):
+                     cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0,
+                     trace=None):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
     tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
     shift backward with the serial schedule on the SMs that whole gangs leave idle (see
-    dash_bwd_options_t)."""
+    dash_bwd_options_t).  ``trace``: optional int64 device tensor [n_tasks, TRACE_SLOTS] that the traced
+    main kernel fills with per-task phase stamps."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
@@ -160,6 +166,8 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     keep = []
     if dq_accum_out is not None:
         opt.dq_accum_out = _dev(dq_accum_out, torch.float32, "dq_accum_out").value
+    if trace is not None:
+        opt.trace = _dev(trace, torch.int64, "trace").value
     if tasks is not None:
         t = np.ascontiguousarray(tasks, dtype=np.int32)
         o_ = np.ascontiguousarray(cta_off, dtype=np.int32)

@@ -241,6 +241,9 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (st != DASH_OK) return st;
   if (opt && opt->dq_accum_out && !aligned16(opt->dq_accum_out))
     return fail(DASH_ERR_INVALID_ARG, "dq_accum_out must be 16-byte aligned");
+  if (opt && opt->trace && (reinterpret_cast<uintptr_t>(opt->trace) & 7u))
+    return fail(DASH_ERR_INVALID_ARG, "trace must be 8-byte aligned");
+  if (opt && opt->trace && T != 128) return fail(DASH_ERR_UNSUPPORTED, "the traced kernel has 128-row tiles only");
   const int n = (S + T - 1) / T;
   std::string why = dash::check_mode(mode, n, causal != 0);
   if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
@@ -405,6 +408,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.spin_limit_ns = spin;
   mp.chains = chains;
   mp.chain_stride = accum_floats;
+  mp.trace = opt ? reinterpret_cast<long long *>(opt->trace) : nullptr;
   if (opt && opt->main_begin_event && (e = cudaEventRecord((cudaEvent_t)opt->main_begin_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
   if ((e = dash::launch_bwd_main(D, T, maps, mp, P, stream)) != cudaSuccess) return cuda_fail(e, "main launch");

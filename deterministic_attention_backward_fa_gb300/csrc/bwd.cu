@@ -137,10 +137,21 @@ __device__ __forceinline__ void regs_set() {
   }
 }
 __device__ __forceinline__ void regs_dec() { regs_set<kRegsProducer>(); }
+// Phase stamp of the traced kernel (compiled out of the plain one).
+template <bool kTrace>
+__device__ __forceinline__ void trace_put(const BwdMainParams &p, int t, int slot, long long v) {
+  if constexpr (kTrace) p.trace[(size_t)t * kTraceSlots + slot] = v;
+}
+__device__ __forceinline__ long long clk() { return clock64(); }
+__device__ __forceinline__ unsigned smid() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
 __device__ __forceinline__ void regs_softmax() { regs_set<kRegsSoftmax>(); }
 __device__ __forceinline__ void regs_reduce() { regs_set<kRegsReduce>(); }
 
-template <int D, int T>
+template <int D, int T, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
     dash_bwd_main(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -324,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bars[bTmemFree], tf_phase, g);
           tf_phase ^= 1;
         }
+        trace_put<kTrace>(p, t, kTrMmaDp, clk());
         if (!*g.abort) {
           tc_fence_after();
           // dP^T = V dO^T
@@ -338,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_wait(&bars[bPFull], pf_phase, g);
         pf_phase ^= 1;
+        trace_put<kTrace>(p, t, kTrMmaDv, clk());
         const uint64_t dQm = sw128_desc(sQ, C::kQPanel, 1024), dDOm = sw128_desc(sDO, C::kQPanel, 1024);
         if (!*g.abort) {
           tc_fence_after();
@@ -373,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait(&bars[bTmemFree], tf_phase, g);
           tf_phase ^= 1;
         }
+        trace_put<kTrace>(p, t, kTrMmaDq, clk());
         if (!*g.abort) {
           tc_fence_after();
           // dQ = dS K first (it is on the critical path: the drain frees the
@@ -396,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&bars[bKvEmpty]);
           }
         }
+        trace_put<kTrace>(p, t, kTrMmaEnd, clk());
         st = (st + 1 == C::kStages) ? 0 : st + 1;
       }
       if (issued) {  // every MMA has completed before tensor memory is released
@@ -425,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       qfq_phase[st] ^= 1;
       mbar_wait(&bars[bSFull], sf_phase, g);
       sf_phase ^= 1;
+      const bool tracer = kTrace && warp == kSoftWarp0 && lane == 0;
+      if (tracer) trace_put<kTrace>(p, t, kTrPassA0, clk());
       float pv[C::kChunks][32];  // P of this thread's row and columns, kept for pass B
       if (!warp_aborted(g)) {
         tc_fence_after();
@@ -464,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
       __syncwarp();
+      if (tracer) trace_put<kTrace>(p, t, kTrPassA1, clk());
       if (lane == 0) {
         mbar_arrive(&bars[bPFull]);
         mbar_arrive(&qemptyQ[st]);  // this warp is done with the stage's LSE
@@ -476,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&bars[bKDone], kd_phase, g);
         kd_phase ^= 1;
       }
+      if (tracer) trace_put<kTrace>(p, t, kTrPassB0, clk());
       if (!warp_aborted(g)) {
         tc_fence_after();
         // pass B: dS = P * (dP - delta), into shared memory as [q/64][kv][64 q]:
@@ -508,6 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
       }
       __syncwarp();
+      if (tracer) trace_put<kTrace>(p, t, kTrPassB1, clk());
       if (lane == 0) {
         mbar_arrive(&bars[bDsFull]);
         mbar_arrive(&qemptyDO[st]);  // this warp is done with the stage's delta
@@ -534,20 +554,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // -------- dQ partial: TMEM -> registers; tensor memory is free at once.
       mbar_wait(&bars[bDqFull], dq_phase, g);
       dq_phase ^= 1;
+      if (kTrace && leader) {
+        trace_put<kTrace>(p, t, kTrRedQ, clk());
+        trace_put<kTrace>(p, t, kTrMeta, (long long)smid() * 65536 + blockIdx.x);
+      }
       float acc[D];
       const bool ok = !warp_aborted(g);
       if (ok) {
         tc_fence_after();
+        // all D columns in flight at once, one wait: the dQ columns are free
+        // (and the next dP^T can go) one load latency after the partial landed
+        uint32_t r[D / 32][32];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld32(tl + C::cDQ + c0, r);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tl + C::cDQ + 32 * c, r[c]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc[c0 + e] = __uint_as_float(r[e]);
+        for (int c = 0; c < D / 32; ++c) {
+          reg_order32(r[c]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc[32 * c + e] = __uint_as_float(r[c][e]);
         }
         tc_fence_before();
       }
       __syncwarp();
+      if (kTrace && leader) trace_put<kTrace>(p, t, kTrRedLd, clk());
       if (lane == 0) mbar_arrive(&bars[bTmemFree]);
       // The tile's turn: acquire the semaphore while the partial waits in
       // registers, so that no shared memory is held during the wait.  With
@@ -557,6 +587,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int *sem = p.sem + (((size_t)bh * p.n + q) * p.chains + chain) * kSemStride;
       float *dst = p.dq_accum + chain * p.chain_stride + ((size_t)bh * p.n + q) * (size_t)(T * D);
       const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
+      if (kTrace && leader) {
+        trace_put<kTrace>(p, t, kTrClkAtAcq0, clk());
+        trace_put<kTrace>(p, t, kTrAcq0, (long long)globaltimer_ns());
+      }
       if (leader && ordered && !*g.abort) {
         const uint64_t t0 = globaltimer_ns();
         // the time limit is checked every 64 polls: a timer read per poll
@@ -576,6 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer (dV, its last reader, completed before dQ) for a bulk
       // reduce-add by the TMA engine, which moves data faster than the
       // vector reductions, and adds the first half from registers meanwhile.
+      if (kTrace && leader) trace_put<kTrace>(p, t, kTrAcq1, (long long)globaltimer_ns());
       named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
       const int red_vecs = ordered ? 2 * kHalfChunks : kHalfChunks;
       if (ordered) {
@@ -628,13 +663,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
       }
+      if (kTrace && leader) trace_put<kTrace>(p, t, kTrRedIssued, clk());
       if (ordered) {
         named_bar(kDrainBar, kRedThreads);  // every thread's reductions are issued
+        if (kTrace && leader) trace_put<kTrace>(p, t, kTrRel0, (long long)globaltimer_ns());
         // The release is cumulative: it covers the other threads' reductions,
         // which the named barrier ordered before it.  Its fence waits until L2
         // has them, so the next rank's adds land after these.
         if (leader && !*g.abort) st_release_gpu(sem, pos + 1);
+      } else if (kTrace && leader) {
+        trace_put<kTrace>(p, t, kTrRel0, (long long)globaltimer_ns());
       }
+      if (kTrace && leader) trace_put<kTrace>(p, t, kTrRel1, (long long)globaltimer_ns());
       // -------- end of a KV run: dK, dV out of TMEM
       if (last) {
         mbar_wait(&bars[bDkvFull], dkvf_phase, g);
@@ -798,10 +838,10 @@ __global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict_
   }
 }
 
-template <int D, int T>
+template <int D, int T, bool kTrace>
 cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_ctas, cudaStream_t stream) {
   using C = BwdCfg<D, T>;
-  auto kfn = dash_bwd_main<D, T>;
+  auto kfn = dash_bwd_main<D, T, kTrace>;
   // The setmaxnreg split above assumes the CTA is launched with exactly
   // kRegsLaunch registers per thread; with fewer, an increase could wait forever.
   cudaFuncAttributes fa;
@@ -849,10 +889,15 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream
 
 cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
                             cudaStream_t stream) {
-  if (D == 64 && T == 64) return launch_main_t<64, 64>(maps, p, num_ctas, stream);
-  if (D == 64 && T == 128) return launch_main_t<64, 128>(maps, p, num_ctas, stream);
-  if (D == 128 && T == 64) return launch_main_t<128, 64>(maps, p, num_ctas, stream);
-  if (D == 128 && T == 128) return launch_main_t<128, 128>(maps, p, num_ctas, stream);
+  if (p.trace) {  // the traced kernel exists for the 128-row tiles only
+    if (D == 64 && T == 128) return launch_main_t<64, 128, true>(maps, p, num_ctas, stream);
+    if (D == 128 && T == 128) return launch_main_t<128, 128, true>(maps, p, num_ctas, stream);
+    return cudaErrorNotSupported;
+  }
+  if (D == 64 && T == 64) return launch_main_t<64, 64, false>(maps, p, num_ctas, stream);
+  if (D == 64 && T == 128) return launch_main_t<64, 128, false>(maps, p, num_ctas, stream);
+  if (D == 128 && T == 64) return launch_main_t<128, 64, false>(maps, p, num_ctas, stream);
+  if (D == 128 && T == 128) return launch_main_t<128, 128, false>(maps, p, num_ctas, stream);
   return cudaErrorInvalidValue;
 }
 

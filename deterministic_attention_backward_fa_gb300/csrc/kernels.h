@@ -50,6 +50,31 @@ struct BwdMainParams {
   long long spin_limit_ns;
   int chains;            // ordered schedules: 1, or 2 (ranks split by parity, one accumulator each)
   long long chain_stride;  // floats between the chains' accumulators
+  long long *trace = nullptr;  // optional [n_tasks][kTraceSlots] phase stamps (traced kernel), else null
+};
+
+// Phase stamps of the traced main kernel, one row of kTraceSlots int64 per
+// task (indexed by the task's position in the table).  "clk" stamps are the
+// SM's clock64, "ns" stamps the global timer.
+enum TraceSlot {
+  kTrMmaDp = 0,      // clk: MMA warp starts dP^T (its waits are over)
+  kTrMmaDv = 1,      // clk: MMA warp has P and starts dV
+  kTrMmaDq = 2,      // clk: MMA warp has dS and starts dQ
+  kTrMmaEnd = 3,     // clk: MMA warp has issued the task's last MMA and commits
+  kTrPassA0 = 4,     // clk: softmax warp 4 has S^T (pass A starts)
+  kTrPassA1 = 5,     // clk: pass A done
+  kTrPassB0 = 6,     // clk: pass B starts (dP^T landed, dS buffer free)
+  kTrPassB1 = 7,     // clk: pass B done
+  kTrRedQ = 8,       // clk: reduction leader sees the dQ partial in tensor memory
+  kTrRedLd = 9,      // clk: the partial is in registers, tensor memory released
+  kTrAcq0 = 10,      // ns: the leader starts waiting for the tile's turn
+  kTrAcq1 = 11,      // ns: the tile's turn has come (semaphore acquired; atomic: at once)
+  kTrRedIssued = 12, // clk: the leader's own reductions are issued
+  kTrRel0 = 13,      // ns: every reduction of the task is issued; the release of rank + 1 starts
+  kTrClkAtAcq0 = 14, // clk read next to kTrAcq0, to put both clocks on one axis
+  kTrMeta = 15,      // smid * 65536 + CTA index
+  kTrRel1 = 16,      // ns: the release store has returned (its fence is done)
+  kTraceSlots = 17
 };
 
 struct BwdPreParams {

@@ -125,7 +125,29 @@ typedef struct {
                             * (dash_check_table; DASH_ERR_SCHEDULE if they could not finish); 1 = bounds
                             * checks only, so that an inconsistent table reaches the device, whose bounded
                             * waits then report DASH_ERR_TIMEOUT (testing). */
+  int64_t *trace;          /* optional device int64 [n_tasks][DASH_TRACE_SLOTS], 8-byte aligned (profiling):
+                            * runs the traced build of the main kernel, which stamps each task's phases
+                            * (slots below) into the row of the task's position in the table.  Same
+                            * results, bit for bit, as the plain kernel.  128-row tiles only
+                            * (DASH_ERR_UNSUPPORTED otherwise). */
 } dash_bwd_options_t;
+
+/* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
+ *  0 clk MMA warp starts dP^T         1 clk MMA warp has P, starts dV
+ *  2 clk MMA warp has dS, starts dQ   3 clk MMA warp has issued the task's last MMA
+ *  4 clk pass A starts (S^T landed)   5 clk pass A done (P in tensor memory)
+ *  6 clk pass B starts                7 clk pass B done (dS in shared memory)
+ *  8 clk dQ partial seen by the reduction warps
+ *  9 clk dQ partial in registers, its tensor memory released
+ * 10 ns  start of the wait for the dQ tile's turn   11 ns  turn taken (semaphore acquired)
+ * 12 clk the reduction leader's adds are issued
+ * 13 ns  every add of the task is issued; the release of rank + 1 starts
+ * 14 clk read next to slot 10 (puts the two clocks on one axis)
+ * 15 smid * 65536 + CTA index
+ * 16 ns  the release store has returned (its fence is done)
+ * (softmax stamps come from softmax warp 4, reduction stamps from the reduction leader;
+ * for the atomic schedule slots 10, 11 and 13 carry no wait) */
+#define DASH_TRACE_SLOTS 17
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
  * checked on the host before the launch: indices in range, runs on one KV tile
