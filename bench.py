@@ -11,7 +11,9 @@ reduction (dq_chains = 2, a different fixed summation order); those figures go
 to `extension_two_dq_chains` and never into `value`.  Shift and symmetric shift
 are also timed with fill (shift_fill = 1: the SMs that whole gangs of their
 chains leave idle run some heads in the serial or descending order), under
-`extension_fill`, never in `value`.  The long causal workload
+`extension_fill`, never in `value`; and with die-aware placement (die_aware = 1:
+each gang of chains on one die, its semaphores homed there) under
+`extension_die_aware`, never in `value`.  The long causal workload
 (causal_s16384_d128) is timed in the same run, every schedule of its mask and
 symmetric shift with fill, and reported under `workloads` with its own ratio
 to atomic and roofline fraction (`--also` names other workloads; '' skips it).
@@ -69,6 +71,8 @@ def parse():
                     help="skip timing the optional two-chain dQ reduction (dq_chains = 2)")
     ap.add_argument("--no-shift-fill", action="store_true",
                     help="skip timing shift and symmetric shift with fill (shift_fill = 1)")
+    ap.add_argument("--no-die-aware", action="store_true",
+                    help="skip timing shift and symmetric shift with die-aware placement (die_aware = 1)")
     ap.add_argument("--also", default="causal_s16384_d128",
                     help="comma-separated further workloads timed in the same run and reported under "
                          "`workloads` (every schedule of the mask and fill; '' for none)")
@@ -224,11 +228,12 @@ def run_reference(args, rank, world):
     return 0
 
 
-def best_with_extensions(results, two_chains, fill, best, world, peak):
-    """The fastest deterministic layout including the two extensions (never in `value`)."""
+def best_with_extensions(results, two_chains, fill, best, world, peak, die=None):
+    """The fastest deterministic layout including the extensions (never in `value`)."""
     cands = {best: results[best]}
     cands.update({f"{s}+fill": r for s, r in fill.items()})
     cands.update({f"{s}+two_dq_chains": r for s, r in two_chains.items()})
+    cands.update({f"{s}+die_aware": r for s, r in (die or {}).items()})
     name = max(cands, key=lambda s: cands[s]["tflops"])
     r = cands[name]
     return {"schedule": name, "tflops": r["tflops"], "ratio_vs_atomic": r.get("vs_atomic"),
@@ -298,9 +303,9 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
     bracketed by CUDA events on the launching stream, with the main kernel's own events inside."""
     q, k, v, o, do, lse, dq, dk, dv = tensors
     flops = w.flops()
-    results, two_chains, fill = {}, {}, {}
+    results, two_chains, fill, die = {}, {}, {}, {}
     launches = 0
-    for sched, chains, shift_fill in runs:
+    for sched, chains, shift_fill, die_aware in runs:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -310,7 +315,7 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         for _ in range(args.warmup):
             flush.fill_(1)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                  dq_chains=chains, shift_fill=shift_fill)
+                                  dq_chains=chains, shift_fill=shift_fill, die_aware=die_aware)
         dash.dash_sync_status()
         barrier()
         torch.cuda.synchronize()
@@ -319,7 +324,7 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
             evs[i][0].record(stream)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
                                   main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
-                                  shift_fill=shift_fill)
+                                  shift_fill=shift_fill, die_aware=die_aware)
             evs[i][3].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -328,10 +333,10 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
         main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
         total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-        (fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
+        (die if die_aware else fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
             "ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
             "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
-    return results, two_chains, fill, launches
+    return results, two_chains, fill, die, launches
 
 
 def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
@@ -342,14 +347,15 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
     o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
     dash.dash_sync_status()
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    runs = [(s, 1, 0) for s in w.schedules]
-    runs += [(s, 1, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
-    results, _, fill, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
-                                           stream, world, dev, barrier)
+    runs = [(s, 1, 0, 0) for s in w.schedules]
+    runs += [(s, 1, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_die_aware]
+    results, _, fill, die, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
+                                                stream, world, dev, barrier)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     atomic = results["atomic"]
-    for r in list(results.values()) + list(fill.values()):
+    for r in list(results.values()) + list(fill.values()) + list(die.values()):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"]
     det = {s: r for s, r in results.items() if s != "atomic"}
     best = max(det, key=lambda s: det[s]["tflops"])
@@ -360,6 +366,7 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
            "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
            "ratio_vs_atomic": results[best]["vs_atomic"], "schedules": results,
            "extension_fill": fill or None,
+           "extension_die_aware": die or None,
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                         "frac": achieved / peak, "kernel": "dash_bwd_main",
                         "peak_source": f"{peak_kind} bf16_tflops (burst)"},
@@ -422,11 +429,13 @@ def main():
             pass
 
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
-    runs = [(s, 1, 0) for s in scheds] + [(s, 2, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
-    runs += [(s, 1, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
+    runs = [(s, 1, 0, 0) for s in scheds]
+    runs += [(s, 2, 0, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
+    runs += [(s, 1, 1, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_die_aware]
     with ClockSampler(gpu_index) as clk:
-        results, two_chains, fill, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args,
-                                                        flush, stream, world, dev, barrier)
+        results, two_chains, fill, die, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
+                                                             args, flush, stream, world, dev, barrier)
         also = {}
         for name in [x for x in args.also.split(",") if x and x != w.name]:
             also[name] = time_other_workload(dash, workloads.WORKLOADS[name], args, flush, stream, world, dev,
@@ -437,7 +446,7 @@ def main():
     det = {s: r for s, r in results.items() if s != "atomic"} or results
     best = max(det, key=lambda s: det[s]["tflops"])
     atomic = results.get("atomic")
-    for s, r in list(results.items()) + list(two_chains.items()) + list(fill.items()):
+    for s, r in list(results.items()) + list(two_chains.items()) + list(fill.items()) + list(die.items()):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
     choice = None
     if atomic and "serial" in results:
@@ -486,7 +495,7 @@ def main():
                        "flops_per_step": flops},
             "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
             "ratio_vs_atomic": results[best]["vs_atomic"],
-            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak),
+            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak, die),
             "schedules": results,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
@@ -496,6 +505,7 @@ def main():
                     "api": "dash_attn_bwd_host (pinned host buffers)"},
             "workloads": also or None,
             "extension_two_dq_chains": two_chains or None,
+            "extension_die_aware": die or None,
             "extension_fill": fill or None,
             "runtime_choice": choice,
             "gpu_launches": launches,

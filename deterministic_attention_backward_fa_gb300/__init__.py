@@ -45,7 +45,7 @@ class BwdOptions(ctypes.Structure):
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
                 ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int),
-                ("trace", ctypes.c_void_p)]
+                ("trace", ctypes.c_void_p), ("die_aware", ctypes.c_int)]
 
 # Slots of a trace row (dash_bwd_options_t.trace): see include/dash.h.
 TRACE_SLOTS = 17
@@ -70,6 +70,9 @@ _SIGS = {
     "dash_check_table": ([_I] * 4 + [_P, _P, _I], _I),
     "dash_fit_costs": ([_I] * 4 + [ctypes.c_double] * 2 + [ctypes.POINTER(_I)] * 2, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
+    "dash_cluster_latencies": ([_P, _I, _I, _P, _P], _I),
+    "dash_place_schedule": ([_P, _P] + [_I] * 5 + [_P, _I, _P, _I, _P, _I, _P, _I, _I, _P, _P], _I),
+    "dash_die_map": ([_P, _P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
     "dash_sync_status": ([_P], _I),
     "dash_release_workspace": ([], None),
     "dash_last_error": ([], ctypes.c_char_p),
@@ -149,13 +152,14 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
                      cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0,
-                     trace=None):
+                     trace=None, die_aware=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
     tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
     shift backward with the serial schedule on the SMs that whole gangs leave idle (see
     dash_bwd_options_t).  ``trace``: optional int64 device tensor [n_tasks, TRACE_SLOTS] that the traced
-    main kernel fills with per-task phase stamps."""
+    main kernel fills with per-task phase stamps.  ``die_aware=1`` places each gang of a shift schedule
+    on one die with its semaphores homed there (see dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
@@ -168,6 +172,7 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
         opt.dq_accum_out = _dev(dq_accum_out, torch.float32, "dq_accum_out").value
     if trace is not None:
         opt.trace = _dev(trace, torch.int64, "trace").value
+    opt.die_aware = die_aware
     if tasks is not None:
         t = np.ascontiguousarray(tasks, dtype=np.int32)
         o_ = np.ascontiguousarray(cta_off, dtype=np.int32)
@@ -264,6 +269,39 @@ def dash_choose_schedule(BH: int, n: int, causal: bool, max_ctas: int, cost_c: i
     if s < 0:
         raise DashError(1, dash_last_error())
     return {v: k for k, v in SCHEDULES.items()}[s], P.value, ms.value
+
+
+def dash_cluster_latencies(lat):
+    """Host-only.  lat: [n_sms, n_lines] latencies (clocks).  Returns (group per SM, home per line)."""
+    L = np.ascontiguousarray(lat, dtype=np.uint32)
+    g = np.zeros(L.shape[0], dtype=np.int32)
+    h = np.zeros(L.shape[1], dtype=np.int32)
+    _check(lib().dash_cluster_latencies(L.ctypes.data_as(ctypes.c_void_p), L.shape[0], L.shape[1],
+                                        g.ctypes.data_as(ctypes.c_void_p), h.ctypes.data_as(ctypes.c_void_p)))
+    return g, h
+
+
+def dash_place_schedule(tasks, cta_off, gang: int, BH: int, n: int, chains: int, smids, lines, max_smid: int):
+    """Host-only.  smids, lines: pairs of int lists (group 0, group 1).  Returns (slot_of_smid, sem_idx)."""
+    t = np.ascontiguousarray(tasks, dtype=np.int32).reshape(-1, 4)
+    o = np.ascontiguousarray(cta_off, dtype=np.int32)
+    a = [np.ascontiguousarray(x, dtype=np.int32) for x in (*smids, *lines)]
+    slot = np.zeros(max_smid + 1, dtype=np.int32)
+    sem = np.zeros(BH * n * chains, dtype=np.int32)
+    p = lambda x: x.ctypes.data_as(ctypes.c_void_p)
+    _check(lib().dash_place_schedule(p(t), p(o), len(o) - 1, gang, BH, n, chains, p(a[0]), len(a[0]), p(a[1]),
+                                     len(a[1]), p(a[2]), len(a[2]), p(a[3]), len(a[3]), max_smid, p(slot), p(sem)))
+    return slot, sem
+
+
+def dash_die_map(max_sm: int = 1023, stream=None):
+    """The device's SM groups as the stream's workspace measures them: (group per SM id, -1 for ids the
+    device does not have; n0, n1)."""
+    g = np.zeros(max_sm + 1, dtype=np.int32)
+    n0, n1 = _I(0), _I(0)
+    _check(lib().dash_die_map(_stream(stream), g.ctypes.data_as(ctypes.c_void_p), max_sm, ctypes.byref(n0),
+                              ctypes.byref(n1)))
+    return g, n0.value, n1.value
 
 
 def dash_sync_status(stream=None):

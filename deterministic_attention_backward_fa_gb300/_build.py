@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdash.so")
 
-SOURCES = ["api.cpp", "schedule.cpp", "bwd.cu", "fwd.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "schedule.cpp", "place.cpp", "bwd.cu", "fwd.cu", "noalloc.cu", "place.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", CSRC, "-I", INCLUDE]
 

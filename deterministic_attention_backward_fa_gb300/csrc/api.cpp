@@ -23,6 +23,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "place.h"
 #include "schedule.h"
 
 namespace {
@@ -137,15 +138,34 @@ struct CopyLanes {
   }
 };
 
+// Die-aware placement (an extension): the SM groups of the two dies and a
+// semaphore pool whose lines' homes are known, measured once per workspace.
+constexpr int kPoolLines = 4096;  // 512 KiB: four 32-byte semaphore sectors per line
+struct DieMap {
+  bool tried = false, ready = false;
+  std::string why;                  // why it is not ready
+  DevBuf pool;                      // kPoolLines lines of 128 bytes
+  std::vector<int> smids[2];        // SM ids per group, ascending
+  std::vector<int> lines[2];        // pool lines homed on each group
+  int max_smid = 0;
+};
+struct PlacementEntry {
+  DevBuf slot_of_smid, sem_idx;
+  int n_smid = 0;
+};
+
 struct Workspace {
   DevBuf accum, lse2, delta, sem, status;
   // device copies used by dash_attn_bwd_host
   DevBuf h_in[6], h_out[3];
   CopyLanes lanes;
+  DieMap die;
+  std::map<std::tuple<int, int, int, int, int, int, int, int, int, int>, std::unique_ptr<PlacementEntry>> placed;
 };
 
 struct ScheduleEntry {
   DevBuf tasks, cta_off;
+  std::vector<int32_t> tasks_h, cta_off_h;  // host copies (die-aware placement reads them)
   int P = 0;
   long long makespan = 0;
 };
@@ -226,6 +246,53 @@ dash_status_t validate_table(const int32_t *tasks, const int32_t *off, int P, in
   return DASH_OK;
 }
 
+// Measures the die map of a workspace once: the latency probe on the call's
+// stream (which it synchronises), then the clustering on the host.
+dash_status_t ensure_die_map(Workspace *w, int sms, cudaStream_t stream) {
+  DieMap &d = w->die;
+  if (d.ready) return DASH_OK;
+  if (d.tried) return fail(DASH_ERR_UNSUPPORTED, "die-aware placement unavailable: %s", d.why.c_str());
+  d.tried = true;
+  DevBuf lat, smid;
+  cudaError_t e;
+  if ((e = d.pool.reserve((size_t)kPoolLines * 128)) != cudaSuccess ||
+      (e = lat.reserve((size_t)sms * kPoolLines * 4)) != cudaSuccess || (e = smid.reserve((size_t)sms * 4)) != cudaSuccess) {
+    d.why = "allocation failed";
+    return fail(DASH_ERR_NO_MEMORY, "die map: %s", cudaGetErrorString(e));
+  }
+  if ((e = dash::launch_probe_homes((unsigned *)d.pool.ptr, kPoolLines, (unsigned *)lat.ptr, (int *)smid.ptr, sms,
+                                    stream)) != cudaSuccess) {
+    d.why = "the latency probe did not launch";
+    return cuda_fail(e, "die map probe");
+  }
+  std::vector<uint32_t> h_lat((size_t)sms * kPoolLines);
+  std::vector<int> h_sm(sms);
+  if ((e = cudaMemcpyAsync(h_lat.data(), lat.ptr, h_lat.size() * 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(h_sm.data(), smid.ptr, h_sm.size() * 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess) {
+    d.why = "the latency probe failed";
+    return cuda_fail(e, "die map probe");
+  }
+  std::vector<int> seen(h_sm);
+  std::sort(seen.begin(), seen.end());
+  if (std::unique(seen.begin(), seen.end()) != seen.end() || seen.front() < 0) {
+    d.why = "the probe did not run one CTA on every SM";
+    return fail(DASH_ERR_UNSUPPORTED, "die-aware placement unavailable: %s", d.why.c_str());
+  }
+  std::vector<int> grp(sms), home(kPoolLines);
+  std::string why = dash::cluster_latencies(h_lat.data(), sms, kPoolLines, grp.data(), home.data());
+  if (!why.empty()) {
+    d.why = why;
+    return fail(DASH_ERR_UNSUPPORTED, "die-aware placement unavailable: %s", why.c_str());
+  }
+  for (int c = 0; c < sms; ++c) d.smids[grp[c]].push_back(h_sm[c]);
+  for (int g = 0; g < 2; ++g) std::sort(d.smids[g].begin(), d.smids[g].end());
+  d.max_smid = seen.back();
+  for (int a = 0; a < kPoolLines; ++a) d.lines[home[a]].push_back(a);
+  d.ready = true;
+  return DASH_OK;
+}
+
 dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *o, const void *dout,
                        const float *lse, void *dq, void *dk, void *dv, int B, int H, int S, int D, int causal,
                        float scale, dash_schedule_t schedule, const dash_bwd_options_t *opt,
@@ -256,6 +323,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1))
     return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
   const bool fill = (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT) && opt && opt->shift_fill == 1;
+  if (opt && (opt->die_aware < 0 || opt->die_aware > 1)) return fail(DASH_ERR_INVALID_ARG, "die_aware must be 0 or 1");
+  const bool die_aware = opt && opt->die_aware == 1;
+  if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks))
+    return fail(DASH_ERR_UNSUPPORTED, "die_aware applies to shift and symmetric shift, without fill or a supplied table");
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -269,6 +340,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const int32_t *dev_tasks = nullptr;
   const int32_t *dev_off = nullptr;
   int P = 0;
+  ScheduleEntry *sched_ent = nullptr;
+  std::tuple<int, int, int, int, int, int, int, int, int, int> sched_key;
   ScheduleEntry custom_holder;  // a caller-supplied table lives for this call only
   if (opt && opt->tasks) {
     if (!opt->cta_off || opt->num_ctas < 1) return fail(DASH_ERR_INVALID_ARG, "tasks needs cta_off and num_ctas");
@@ -335,11 +408,15 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       }
       fresh->P = Puse;
       fresh->makespan = sch.makespan;
+      fresh->tasks_h = std::move(sch.tasks);
+      fresh->cta_off_h = std::move(sch.cta_off);
       ent = std::move(fresh);
     }
     dev_tasks = (const int32_t *)ent->tasks.ptr;
     dev_off = (const int32_t *)ent->cta_off.ptr;
     P = ent->P;
+    sched_ent = ent.get();
+    sched_key = key;
   }
 
   // ---- workspace
@@ -353,6 +430,36 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       (e = w->sem.reserve_on((size_t)BH * n * chains * dash::kSemStride * 4, stream)) != cudaSuccess ||
       (e = ensure_status(w)) != cudaSuccess)
     return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
+
+  // ---- die-aware placement: each gang on one die, its semaphores homed there
+  PlacementEntry *placed = nullptr;
+  if (die_aware) {
+    if ((st = ensure_die_map(w, sms, stream)) != DASH_OK) return st;
+    auto &pe = w->placed[sched_key];
+    if (!pe) {
+      dash::Placement plc;
+      why = dash::build_placement(sched_ent->tasks_h.data(), sched_ent->cta_off_h.data(), P,
+                                  dash::chains_per_head(mode, n), BH, n, chains, w->die.smids, w->die.lines,
+                                  w->die.max_smid, &plc);
+      if (!why.empty()) {
+        w->placed.erase(sched_key);
+        return fail(DASH_ERR_UNSUPPORTED, "die-aware placement: %s", why.c_str());
+      }
+      std::unique_ptr<PlacementEntry> fresh(new PlacementEntry());
+      if ((e = fresh->slot_of_smid.reserve(plc.slot_of_smid.size() * 4)) != cudaSuccess ||
+          (e = fresh->sem_idx.reserve(plc.sem_idx.size() * 4)) != cudaSuccess ||
+          (e = cudaMemcpy(fresh->slot_of_smid.ptr, plc.slot_of_smid.data(), plc.slot_of_smid.size() * 4,
+                          cudaMemcpyHostToDevice)) != cudaSuccess ||
+          (e = cudaMemcpy(fresh->sem_idx.ptr, plc.sem_idx.data(), plc.sem_idx.size() * 4, cudaMemcpyHostToDevice)) !=
+              cudaSuccess) {
+        w->placed.erase(sched_key);
+        return cuda_fail(e, "die-aware placement tables");
+      }
+      fresh->n_smid = (int)plc.slot_of_smid.size();
+      pe = std::move(fresh);
+    }
+    placed = pe.get();
+  }
 
   // ---- tensor maps
   dash::BwdMaps maps;
@@ -381,8 +488,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   } else {
     pre.accum_floats = accum_floats * chains;
   }
-  pre.sem = (int *)w->sem.ptr;
-  pre.sem_count = BH * n * chains * dash::kSemStride;
+  pre.sem = placed ? (int *)w->die.pool.ptr : (int *)w->sem.ptr;
+  pre.sem_count = placed ? kPoolLines * 32 : BH * n * chains * dash::kSemStride;
   pre.S = S;
   pre.D = D;
   pre.rows_padded = (int)rows_padded;
@@ -409,9 +516,16 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.chains = chains;
   mp.chain_stride = accum_floats;
   mp.trace = opt ? reinterpret_cast<long long *>(opt->trace) : nullptr;
+  if (placed) {
+    mp.slot_of_smid = (const int *)placed->slot_of_smid.ptr;
+    mp.n_smid = placed->n_smid;
+    mp.sem_idx = (const int *)placed->sem_idx.ptr;
+  }
   if (opt && opt->main_begin_event && (e = cudaEventRecord((cudaEvent_t)opt->main_begin_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
-  if ((e = dash::launch_bwd_main(D, T, maps, mp, P, stream)) != cudaSuccess) return cuda_fail(e, "main launch");
+  // die-aware: one CTA per SM, each running the slot of its SM
+  if ((e = dash::launch_bwd_main(D, T, maps, mp, placed ? sms : P, stream)) != cudaSuccess)
+    return cuda_fail(e, "main launch");
   if (opt && opt->main_end_event && (e = cudaEventRecord((cudaEvent_t)opt->main_end_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
   if ((e = dash::launch_bwd_convert(D, T, accum, chains, accum_floats, dq, opt ? opt->dq_accum_out : nullptr,
@@ -627,6 +741,59 @@ int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, in
   return s;
 }
 
+dash_status_t dash_cluster_latencies(const uint32_t *lat, int n_sms, int n_lines, int32_t *group_out,
+                                     int32_t *home_out) {
+  if (!lat || !group_out || !home_out || n_sms < 2 || n_lines < 1)
+    return fail(DASH_ERR_INVALID_ARG, "dash_cluster_latencies: null pointer or sizes too small");
+  std::vector<int> g(n_sms), h(n_lines);
+  const std::string why = dash::cluster_latencies(lat, n_sms, n_lines, g.data(), h.data());
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::copy(g.begin(), g.end(), group_out);
+  std::copy(h.begin(), h.end(), home_out);
+  return DASH_OK;
+}
+
+dash_status_t dash_place_schedule(const int32_t *tasks, const int32_t *cta_off, int P, int gang, int BH, int n,
+                                  int chains, const int32_t *sm0, int n0, const int32_t *sm1, int n1,
+                                  const int32_t *line0, int m0, const int32_t *line1, int m1, int max_smid,
+                                  int32_t *slot_of_smid_out, int32_t *sem_idx_out) {
+  if (!tasks || !cta_off || !slot_of_smid_out || !sem_idx_out || (n0 && !sm0) || (n1 && !sm1) || (m0 && !line0) ||
+      (m1 && !line1) || n0 < 0 || n1 < 0 || m0 < 0 || m1 < 0)
+    return fail(DASH_ERR_INVALID_ARG, "dash_place_schedule: null pointer or negative size");
+  const std::vector<int> smids[2] = {std::vector<int>(sm0, sm0 + n0), std::vector<int>(sm1, sm1 + n1)};
+  const std::vector<int> lines[2] = {std::vector<int>(line0, line0 + m0), std::vector<int>(line1, line1 + m1)};
+  for (int g = 0; g < 2; ++g)
+    for (int x : smids[g])
+      if (x < 0 || x > max_smid) return fail(DASH_ERR_INVALID_ARG, "SM id %d outside [0, %d]", x, max_smid);
+  dash::Placement plc;
+  const std::string why = dash::build_placement(tasks, cta_off, P, gang, BH, n, chains, smids, lines, max_smid, &plc);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::copy(plc.slot_of_smid.begin(), plc.slot_of_smid.end(), slot_of_smid_out);
+  std::copy(plc.sem_idx.begin(), plc.sem_idx.end(), sem_idx_out);
+  return DASH_OK;
+}
+
+dash_status_t dash_die_map(dash_stream_t stream_, int32_t *group_of_smid_out, int max_sm, int *n0, int *n1) {
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (!group_of_smid_out || max_sm < 0) return fail(DASH_ERR_INVALID_ARG, "dash_die_map: null pointer");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(g_mu);
+  const int sms = sm_count(dev);
+  if (sms <= 0) return fail(DASH_ERR_CUDA, "cannot query the SM count");
+  Workspace *w = workspace(dev, stream);
+  dash_status_t st = ensure_die_map(w, sms, stream);
+  if (st != DASH_OK) return st;
+  for (int i = 0; i <= max_sm; ++i) group_of_smid_out[i] = -1;
+  for (int g = 0; g < 2; ++g)
+    for (int x : w->die.smids[g])
+      if (x <= max_sm) group_of_smid_out[x] = g;
+  if (n0) *n0 = (int)w->die.smids[0].size();
+  if (n1) *n1 = (int)w->die.smids[1].size();
+  return DASH_OK;
+}
+
 dash_status_t dash_sync_status(dash_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   cudaError_t e = cudaStreamSynchronize(stream);
@@ -660,6 +827,6 @@ void dash_release_workspace(void) {
 
 const char *dash_last_error(void) { return g_last_error.c_str(); }
 
-int dash_version(void) { return 100; }
+int dash_version(void) { return 200; }
 
 }  // extern "C"

@@ -160,6 +160,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // With die-aware placement every SM holds one CTA, which runs the slot that
+  // the host gave its SM (or nothing, before any set-up).
+  int slot = blockIdx.x;
+  if (p.slot_of_smid) {
+    const int s = (int)smid();
+    slot = s < p.n_smid ? p.slot_of_smid[s] : -1;
+    if (slot < 0) return;
+  }
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::oBAR);
   uint64_t *qfullQ = bars + bQFull0;                   // Q tile + LSE landed
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Guard g{abort_flag, p.status, (uint64_t)p.spin_limit_ns};
 
-  const int t_begin = p.cta_off[blockIdx.x], t_end = p.cta_off[blockIdx.x + 1];
+  const int t_begin = p.cta_off[slot], t_end = p.cta_off[slot + 1];
   const int4 *tasks = p.tasks;
 
   if (warp < 4) {
@@ -556,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dq_phase ^= 1;
       if (kTrace && leader) {
         trace_put<kTrace>(p, t, kTrRedQ, clk());
-        trace_put<kTrace>(p, t, kTrMeta, (long long)smid() * 65536 + blockIdx.x);
+        trace_put<kTrace>(p, t, kTrMeta, (long long)smid() * 65536 + slot);
       }
       float acc[D];
       const bool ok = !warp_aborted(g);
@@ -584,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // two chains, even ranks add into the first accumulator and odd ranks
       // into the second, each in rank order behind its own semaphore.
       const int chain = ordered ? rank % p.chains : 0, pos = ordered ? rank / p.chains : 0;
-      int *sem = p.sem + (((size_t)bh * p.n + q) * p.chains + chain) * kSemStride;
+      const size_t sem_key = ((size_t)bh * p.n + q) * p.chains + chain;
+      int *sem = p.sem + (p.sem_idx ? (size_t)p.sem_idx[sem_key] : sem_key * kSemStride);
       float *dst = p.dq_accum + chain * p.chain_stride + ((size_t)bh * p.n + q) * (size_t)(T * D);
       const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
       if (kTrace && leader) {

@@ -51,6 +51,12 @@ struct BwdMainParams {
   int chains;            // ordered schedules: 1, or 2 (ranks split by parity, one accumulator each)
   long long chain_stride;  // floats between the chains' accumulators
   long long *trace = nullptr;  // optional [n_tasks][kTraceSlots] phase stamps (traced kernel), else null
+  // Die-aware placement (optional): the CTA on SM s runs slot slot_of_smid[s]
+  // (-1: none; the launch then has one CTA per SM), and the semaphore of
+  // (head, tile, chain) k sits at sem + sem_idx[k] instead of k * kSemStride.
+  const int *slot_of_smid = nullptr;
+  int n_smid = 0;
+  const int *sem_idx = nullptr;
 };
 
 // Phase stamps of the traced main kernel, one row of kTraceSlots int64 per
@@ -72,7 +78,7 @@ enum TraceSlot {
   kTrRedIssued = 12, // clk: the leader's own reductions are issued
   kTrRel0 = 13,      // ns: every reduction of the task is issued; the release of rank + 1 starts
   kTrClkAtAcq0 = 14, // clk read next to kTrAcq0, to put both clocks on one axis
-  kTrMeta = 15,      // smid * 65536 + CTA index
+  kTrMeta = 15,      // smid * 65536 + the CTA's slot (its task list)
   kTrRel1 = 16,      // ns: the release store has returned (its fence is done)
   kTraceSlots = 17
 };
@@ -106,6 +112,11 @@ cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainPara
 cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
                                float *acc_out, float scale, int BH,
                                int S, int n, int num_sms, cudaStream_t stream);
+
+// Latency probe of the die-aware placement: lat[cta][line] for one CTA per SM
+// over n_lines 128-byte lines of `pool` (which it overwrites), smid_out[cta].
+cudaError_t launch_probe_homes(unsigned *pool, int n_lines, unsigned *lat, int *smid_out, int num_sms,
+                               cudaStream_t stream);
 
 // Forward: Q/K/V maps with 128-row boxes.
 cudaError_t launch_fwd(int D, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -130,6 +130,15 @@ typedef struct {
                             * (slots below) into the row of the task's position in the table.  Same
                             * results, bit for bit, as the plain kernel.  128-row tiles only
                             * (DASH_ERR_UNSUPPORTED otherwise). */
+  int die_aware;           /* DASH_SCHED_SHIFT and DASH_SCHED_SYMMETRIC_SHIFT without fill or a supplied table:
+                            * 0 = CTAs as the hardware places them; 1 = die-aware placement (an extension):
+                            * the main kernel runs one CTA per SM, and each SM takes the task list the host
+                            * gave it, so that every whole gang of chains runs on SMs of one die, and each dQ
+                            * tile's semaphore sits in an L2 line homed on the die that runs most of its adds.
+                            * The first such call on a (device, stream) measures the die map (a probe kernel
+                            * of a few milliseconds, and a synchronisation of the stream).  The tasks, ranks
+                            * and adds are those of the plain schedule, so the results are the same bits.
+                            * DASH_ERR_UNSUPPORTED when the map shows no two groups of SMs. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
@@ -143,7 +152,7 @@ typedef struct {
  * 12 clk the reduction leader's adds are issued
  * 13 ns  every add of the task is issued; the release of rank + 1 starts
  * 14 clk read next to slot 10 (puts the two clocks on one axis)
- * 15 smid * 65536 + CTA index
+ * 15 smid * 65536 + the CTA's slot (its task list)
  * 16 ns  the release store has returned (its fence is done)
  * (softmax stamps come from softmax warp 4, reduction stamps from the reduction leader;
  * for the atomic schedule slots 10, 11 and 13 carry no wait) */
@@ -284,6 +293,42 @@ int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, in
  * positive.  Host only. */
 dash_status_t dash_fit_costs(int BH, int n, int causal, int max_ctas, double atomic_ms, double serial_ms,
                              int *cost_c_out, int *cost_r_out);
+
+/* Die-aware placement, host half (an extension; DASH news (nachedeu.com) on
+ * signalling through a remote L2 segment).  lat holds [n_sms][n_lines] L2 load
+ * latencies in clocks, as the library's probe measures them (one row per SM,
+ * one column per 128-byte line).  Splits the SMs in two groups by two-means
+ * clustering of their rows (started from the split at the line with the
+ * largest spread; at most 20 rounds) and gives each line the group whose mean
+ * latency to it is lower (ties to group 0): group_out[n_sms], home_out[n_lines]
+ * in {0, 1}.  DASH_ERR_SCHEDULE when no split into two groups exists;
+ * DASH_ERR_INVALID_ARG for null pointers or n_sms < 2.  Host only. */
+dash_status_t dash_cluster_latencies(const uint32_t *lat, int n_sms, int n_lines, int32_t *group_out,
+                                     int32_t *home_out);
+
+/* Die-aware placement, tables (host only).  For a task table on P slots
+ * (tasks: 4 int32 per task; cta_off: P + 1), SM ids per group (sm0[n0],
+ * sm1[n1]) and pool lines per home (line0[m0], line1[m1]; 128-byte lines):
+ *  - slot_of_smid_out[max_smid + 1]: the slot each SM runs, -1 for none.  Each
+ *    whole gang of `gang` consecutive slots goes to the group with the most
+ *    SMs left that can hold it (ties to group 0); slots that no group can take
+ *    as a whole gang go to the SMs left, group 0 first;
+ *  - sem_idx_out[BH * n * chains]: the int offset, from the pool base, of the
+ *    semaphore of (head, dQ tile, chain): a 32-byte sector of a line homed on
+ *    the group that runs most of the tile's adds (ties to group 0), taken in
+ *    order, four sectors per line.
+ * DASH_ERR_SCHEDULE when the SMs or pool lines do not suffice. */
+dash_status_t dash_place_schedule(const int32_t *tasks, const int32_t *cta_off, int P, int gang, int BH, int n,
+                                  int chains, const int32_t *sm0, int n0, const int32_t *sm1, int n1,
+                                  const int32_t *line0, int m0, const int32_t *line1, int m1, int max_smid,
+                                  int32_t *slot_of_smid_out, int32_t *sem_idx_out);
+
+/* The die map of the calling thread's current device as the stream's
+ * workspace measures it (the probe runs on `stream` the first time, which is
+ * synchronised): group_of_smid_out[max_sm + 1] receives 0 or 1 for each SM id
+ * (-1 for ids the device does not have), and n0 / n1 the group sizes.
+ * DASH_ERR_UNSUPPORTED if no two groups were found. */
+dash_status_t dash_die_map(dash_stream_t stream, int32_t *group_of_smid_out, int max_sm, int *n0, int *n1);
 
 /* Synchronises `stream` and returns the device status of the calling
  * thread's current device workspace for that stream: DASH_OK, or
