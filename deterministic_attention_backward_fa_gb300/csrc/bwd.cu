@@ -747,50 +747,52 @@ __global__ void __launch_bounds__(256) dash_bwd_preprocess(const __nv_bfloat16 *
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   for (long long i = gtid; i < accum_vec4; i += nthreads) dq_accum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (long long i = gtid; i < sem_count; i += nthreads) sem[i] = 0;
-  // one warp per padded row, two rows per round so that two rows' loads are in
-  // flight at once (the kernel is bound by how many bytes each SM has in flight)
-  const int lane = threadIdx.x & 31;
+  // Each lane reads 16 bytes (8 elements) of a row of O and of dO, so a row is
+  // D / 8 lanes and one load instruction covers 32 / (D / 8) rows; kU of them
+  // per round keep 2 x kU x 16 bytes in flight per lane, which the kernel, bound
+  // by the bytes each SM has in flight, needs to approach HBM bandwidth.
+  constexpr int kLanesPerRow = D / 8;
+  constexpr int kRowsPerLoad = 32 / kLanesPerRow;
+  constexpr int kU = 4;
+  constexpr int kRowsPerRound = kRowsPerLoad * kU;
+  const int lane = threadIdx.x & 31, sub = lane / kLanesPerRow, li = lane % kLanesPerRow;
   const long long gwarp = gtid >> 5, nwarps = nthreads >> 5;
-  constexpr int kPer = D / 32;  // elements per lane
-  constexpr int kRows = 2;
-  for (long long row0 = gwarp * kRows; row0 < total_rows; row0 += nwarps * kRows) {
-    float sum[kRows], l2[kRows];
+  for (long long row0 = gwarp * kRowsPerRound; row0 < total_rows; row0 += nwarps * kRowsPerRound) {
+    uint4 a[kU], b[kU];
+    float l2[kU];
+    bool valid[kU];
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
-      const long long row = row0 + j;
+    for (int u = 0; u < kU; ++u) {
+      const long long row = row0 + u * kRowsPerLoad + sub;
       const long long bh = row / rows_padded;
       const int r = (int)(row - bh * rows_padded);
-      sum[j] = 0.f;
-      l2[j] = __int_as_float(0x7f800000);  // +inf: P = 0 for padded rows
-      if (row < total_rows && r < S) {
-        const size_t base = ((size_t)bh * S + r) * D + lane * kPer;
-        if constexpr (kPer == 4) {
-          const uint2 a = *reinterpret_cast<const uint2 *>(o + base);
-          const uint2 b = *reinterpret_cast<const uint2 *>(dout + base);
-          const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-          const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
-            sum[j] = fmaf(fa.x, fb.x, sum[j]);
-            sum[j] = fmaf(fa.y, fb.y, sum[j]);
-          }
-        } else {
-          const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(o + base);
-          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(dout + base);
-          const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-          sum[j] = fmaf(fa.x, fb.x, fa.y * fb.y);
-        }
-        l2[j] = lse[(size_t)bh * S + r] * 1.4426950408889634f;
+      valid[u] = row < total_rows && r < S;
+      a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+      l2[u] = __int_as_float(0x7f800000);  // +inf: P = 0 for padded rows
+      if (valid[u]) {
+        const size_t base = ((size_t)bh * S + r) * D + li * 8;
+        a[u] = *reinterpret_cast<const uint4 *>(o + base);
+        b[u] = *reinterpret_cast<const uint4 *>(dout + base);
+        if (li == 0) l2[u] = lse[(size_t)bh * S + r] * 1.4426950408889634f;
       }
     }
 #pragma unroll
-    for (int j = 0; j < kRows; ++j) {
+    for (int u = 0; u < kU; ++u) {
+      const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a[u]);
+      const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b[u]);
+      float sum = 0.f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum[j] += __shfl_xor_sync(0xffffffffu, sum[j], off);
-      if (lane == 0 && row0 + j < total_rows) {
-        delta[row0 + j] = sum[j];
-        lse2[row0 + j] = l2[j];
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+        sum = fmaf(fa.x, fb.x, sum);
+        sum = fmaf(fa.y, fb.y, sum);
+      }
+#pragma unroll
+      for (int off = kLanesPerRow / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      const long long row = row0 + u * kRowsPerLoad + sub;
+      if (li == 0 && row < total_rows) {
+        delta[row] = sum;
+        lse2[row] = l2[u];
       }
     }
   }
