@@ -58,6 +58,7 @@ _F = ctypes.c_float
 
 _SIGS = {
     "dash_attn_fwd": ([_P] * 5 + [_I] * 5 + [_F, _P], _I),
+    "dash_attn_fwd_ex": ([_P] * 5 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_attn_bwd": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
     "dash_attn_bwd_ex": ([_P] * 9 + [_I] * 5 + [_F, _I, ctypes.POINTER(BwdOptions), _P], _I),
     "dash_attn_bwd_host": ([_P] * 9 + [_I] * 5 + [_F, _I, _P], _I),
@@ -138,6 +139,15 @@ def dash_attn_fwd(q, k, v, o, lse, causal: bool, scale: float, stream=None):
     _check(lib().dash_attn_fwd(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
                                _dev(lse, torch.float32, "lse"), B, H, S, D, int(causal), float(scale),
                                _stream(stream)))
+
+
+def dash_attn_fwd_ex(q, k, v, o, lse, causal: bool, scale: float, cta_pair: int = -1, stream=None):
+    """``cta_pair``: 0 = one CTA per Q tile, 1 = CTA-pair (cta_group::2) kernel (D = 128), -1 = default."""
+    B, H, S, D = _shape(q)
+    bf = torch.bfloat16
+    _check(lib().dash_attn_fwd_ex(_dev(q, bf, "q"), _dev(k, bf, "k"), _dev(v, bf, "v"), _dev(o, bf, "o"),
+                                  _dev(lse, torch.float32, "lse"), B, H, S, D, int(causal), float(scale),
+                                  int(cta_pair), _stream(stream)))
 
 
 def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, stream=None):
@@ -321,13 +331,16 @@ def dash_version() -> int:
 
 
 # ------------------------------------------------------------ conveniences
-def attn_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None):
+def attn_fwd(q, k, v, causal: bool, scale: float | None = None, stream=None, cta_pair: int = -1):
     """O (bf16) and LSE (fp32, natural log) of softmax attention."""
     B, H, S, D = _shape(q)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    dash_attn_fwd(q, k, v, o, lse, causal, scale, stream)
+    if cta_pair == -1:
+        dash_attn_fwd(q, k, v, o, lse, causal, scale, stream)
+    else:
+        dash_attn_fwd_ex(q, k, v, o, lse, causal, scale, cta_pair, stream)
     return o, lse
 
 

@@ -45,6 +45,8 @@ dash_status_t cuda_fail(cudaError_t e, const char *what) {
 }
 
 constexpr long long kDefaultSpinNs = 2000000000LL;  // 2 s bound on every device wait
+// dash_attn_fwd at D = 128: the CTA-pair kernel (tcgen05 cta_group::2) or the single-CTA one.
+constexpr bool kPairForwardByDefault = false;
 
 // ------------------------------------------------------------ tensor maps
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -547,11 +549,14 @@ bool encode_bhsd_map(CUtensorMap *m, const void *base, int BH, int S, int D, int
 
 extern "C" {
 
-dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int S,
-                            int D, int causal, float scale, dash_stream_t stream_) {
+dash_status_t dash_attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                               int S, int D, int causal, float scale, int cta_pair, dash_stream_t stream_) {
   cudaStream_t stream = (cudaStream_t)stream_;
   dash_status_t st = check_common(B, H, S, D, scale);
   if (st != DASH_OK) return st;
+  if (cta_pair < -1 || cta_pair > 1) return fail(DASH_ERR_INVALID_ARG, "cta_pair must be -1, 0 or 1");
+  if (cta_pair == 1 && D != 128) return fail(DASH_ERR_UNSUPPORTED, "the CTA-pair forward needs D = 128");
+  const bool pair = cta_pair == 1 || (cta_pair == -1 && D == 128 && kPairForwardByDefault);
   const int BH = B * H;
   if (BH == 0 || S == 0) return DASH_OK;
   if ((st = check_ptrs({q, k, v, o, lse})) != DASH_OK) return st;
@@ -563,7 +568,7 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
   if ((e = ensure_status(w)) != cudaSuccess) return fail(DASH_ERR_NO_MEMORY, "status word allocation failed");
   CUtensorMap mq, mk, mv;
   if ((st = make_map(&mq, q, BH, S, D, 128)) != DASH_OK) return st;
-  if ((st = make_map(&mk, k, BH, S, D, 128)) != DASH_OK) return st;
+  if ((st = make_map(&mk, k, BH, S, D, pair ? 64 : 128)) != DASH_OK) return st;  // a pair's CTA loads half a K tile
   if ((st = make_map(&mv, v, BH, S, D, 128)) != DASH_OK) return st;
   dash::FwdParams p;
   p.o = (__nv_bfloat16 *)o;
@@ -573,8 +578,14 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal ? 1 : 0;
   p.spin_limit_ns = kDefaultSpinNs;
-  if ((e = dash::launch_fwd(D, mq, mk, mv, p, BH, stream)) != cudaSuccess) return cuda_fail(e, "forward launch");
+  e = pair ? dash::launch_fwd_pair(mq, mk, mv, p, BH, stream) : dash::launch_fwd(D, mq, mk, mv, p, BH, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return DASH_OK;
+}
+
+dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H, int S,
+                            int D, int causal, float scale, dash_stream_t stream) {
+  return dash_attn_fwd_ex(q, k, v, o, lse, B, H, S, D, causal, scale, -1, stream);
 }
 
 dash_status_t dash_attn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,

@@ -118,6 +118,11 @@ cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long 
 cudaError_t launch_probe_homes(unsigned *pool, int n_lines, unsigned *lat, int *smid_out, int num_sms,
                                cudaStream_t stream);
 
+// CTA-pair forward for D = 128 (tcgen05 cta_group::2): Q and V maps with
+// 128-row boxes, K with 64-row boxes (each CTA of a pair loads half a tile).
+cudaError_t launch_fwd_pair(const CUtensorMap &q, const CUtensorMap &k_half_rows, const CUtensorMap &v,
+                            const FwdParams &p, int BH, cudaStream_t stream);
+
 // Forward: Q/K/V maps with 128-row boxes.
 cudaError_t launch_fwd(int D, const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                        const FwdParams &p, int BH, cudaStream_t stream);

@@ -83,6 +83,16 @@ dash_status_t dash_attn_fwd(const void *q, const void *k, const void *v, void *o
                             int B, int H, int S, int D, int causal, float scale,
                             dash_stream_t stream);
 
+/* dash_attn_fwd with a choice of kernel.  cta_pair = 0: one CTA per 128-row Q
+ * tile; 1: a pair of CTAs (a cluster of two) per two Q tiles, whose MMAs are
+ * tcgen05 CTA-pair MMAs (cta_group::2, M = 256): each CTA loads half of every
+ * K and V tile and the pair's first CTA issues the MMAs (D = 128 only,
+ * DASH_ERR_UNSUPPORTED otherwise); -1: the library's default for D.  The
+ * results agree within rounding (the same sums, formed by other MMA shapes). */
+dash_status_t dash_attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int H, int S, int D, int causal, float scale, int cta_pair,
+                               dash_stream_t stream);
+
 /* Attention backward (DASH overview, section 2.1; Sintesi Tecnica DASH,
  * section 1).  With P as above, dP = dO V^T, delta_i = dO_i.O_i,
  * dS = P*(dP - delta):  dv = P^T dO, dk = scale * dS^T Q, dq = scale * dS K,
