@@ -2,13 +2,17 @@
 head dimension 64 and 128, both masks (24 configurations, every schedule valid
 for the mask).
 
-Each configuration is checked through the C ABI on sampled rows of two heads
-(the first and the last): O and LSE at sampled query rows, dQ at sampled query
-rows and dK, dV at sampled key rows, all against the row-wise fp64 oracle,
-which computes each row from the definition without forming an S x S matrix.
-The rows include the first and last of the sequence and both sides of a tile
-boundary.  Every deterministic schedule must also give the same bits twice.
+Each configuration is checked through the C ABI on sampled rows of four heads
+(the first, the last and two drawn from a seeded generator): O and LSE at
+sampled query rows, dQ at sampled query rows and dK, dV at sampled key rows,
+all against the row-wise fp64 oracle, which computes each row from the
+definition without forming an S x S matrix.  The rows are the first and last
+of the sequence, both sides of a tile boundary, one in the middle, and eight
+drawn from the seeded generator per configuration, so that tile-local errors
+away from those fixed rows are caught.  Every deterministic schedule must also
+give the same bits twice.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -35,8 +39,10 @@ def test_pages_sweep_sampled_rows(w):
     q, k, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
     o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
     dash.dash_sync_status()
-    heads = sorted({(0, 0), (w.B - 1, w.H - 1)})
-    rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1})
+    rng = np.random.default_rng(w.S * 1000 + w.D + (1 if w.causal else 0))
+    extra = rng.choice(w.B * w.H, size=min(2, w.B * w.H), replace=False)
+    heads = sorted({(0, 0), (w.B - 1, w.H - 1)} | {(int(x) // w.H, int(x) % w.H) for x in extra})
+    rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1} | {int(x) for x in rng.integers(0, w.S, 8)})
     refs = {}
     for (b, h) in heads:
         qh, kh, vh, doh = (x[b, h].double().cpu().numpy() for x in (q, k, v, do))
