@@ -45,7 +45,7 @@ class BwdOptions(ctypes.Structure):
                 ("dq_accum_out", ctypes.c_void_p), ("tasks", ctypes.c_void_p), ("cta_off", ctypes.c_void_p),
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
                 ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int),
-                ("trace", ctypes.c_void_p), ("die_aware", ctypes.c_int)]
+                ("trace", ctypes.c_void_p), ("die_aware", ctypes.c_int), ("cluster_size", ctypes.c_int)]
 
 # Slots of a trace row (dash_bwd_options_t.trace): see include/dash.h.
 TRACE_SLOTS = 17
@@ -74,6 +74,7 @@ _SIGS = {
     "dash_cluster_latencies": ([_P, _I, _I, _P, _P], _I),
     "dash_place_schedule": ([_P, _P] + [_I] * 5 + [_P, _I, _P, _I, _P, _I, _P, _I, _I, _P, _P], _I),
     "dash_die_map": ([_P, _P, _I, ctypes.POINTER(_I), ctypes.POINTER(_I)], _I),
+    "dash_cluster_links": ([_P, _P] + [_I] * 5 + [_P, ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_sync_status": ([_P], _I),
     "dash_release_workspace": ([], None),
     "dash_last_error": ([], ctypes.c_char_p),
@@ -162,14 +163,15 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
                      cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0,
-                     trace=None, die_aware=0):
+                     trace=None, die_aware=0, cluster_size=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
     tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
     shift backward with the serial schedule on the SMs that whole gangs leave idle (see
     dash_bwd_options_t).  ``trace``: optional int64 device tensor [n_tasks, TRACE_SLOTS] that the traced
     main kernel fills with per-task phase stamps.  ``die_aware=1`` places each gang of a shift schedule
-    on one die with its semaphores homed there (see dash_bwd_options_t)."""
+    on one die with its semaphores homed there; ``cluster_size`` (0 or 1 = none; 2, 4, 8, 16) sets the thread-block
+    clusters whose ranks hand the dQ turn over through shared memory (see dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
@@ -183,6 +185,7 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     if trace is not None:
         opt.trace = _dev(trace, torch.int64, "trace").value
     opt.die_aware = die_aware
+    opt.cluster_size = cluster_size
     if tasks is not None:
         t = np.ascontiguousarray(tasks, dtype=np.int32)
         o_ = np.ascontiguousarray(cta_off, dtype=np.int32)
@@ -302,6 +305,18 @@ def dash_place_schedule(tasks, cta_off, gang: int, BH: int, n: int, chains: int,
     _check(lib().dash_place_schedule(p(t), p(o), len(o) - 1, gang, BH, n, chains, p(a[0]), len(a[0]), p(a[1]),
                                      len(a[1]), p(a[2]), len(a[2]), p(a[3]), len(a[3]), max_smid, p(slot), p(sem)))
     return slot, sem
+
+
+def dash_cluster_links(tasks, cta_off, C: int, BH: int, n: int, chains: int = 1):
+    """Host-only.  Returns (link word per task, number of linked hand-offs) for clusters of C."""
+    t = np.ascontiguousarray(tasks, dtype=np.int32).reshape(-1, 4)
+    o = np.ascontiguousarray(cta_off, dtype=np.int32)
+    out = np.zeros(len(t), dtype=np.int32)
+    k = ctypes.c_longlong(0)
+    _check(lib().dash_cluster_links(t.ctypes.data_as(ctypes.c_void_p), o.ctypes.data_as(ctypes.c_void_p),
+                                    len(o) - 1, C, BH, n, chains, out.ctypes.data_as(ctypes.c_void_p),
+                                    ctypes.byref(k)))
+    return out, int(k.value)
 
 
 def dash_die_map(max_sm: int = 1023, stream=None):

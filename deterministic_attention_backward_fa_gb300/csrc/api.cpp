@@ -167,9 +167,11 @@ struct Workspace {
 
 struct ScheduleEntry {
   DevBuf tasks, cta_off;
-  std::vector<int32_t> tasks_h, cta_off_h;  // host copies (die-aware placement reads them)
+  std::vector<int32_t> tasks_h, cta_off_h;  // host copies (die-aware placement and cluster links read them)
   int P = 0;
   long long makespan = 0;
+  std::map<std::pair<int, int>, int> cluster_for;      // (D, tile) -> cluster size that fits
+  std::map<int, std::unique_ptr<DevBuf>> linked_for;   // cluster size -> device task table with the links merged
 };
 
 std::mutex g_mu;
@@ -329,6 +331,9 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const bool die_aware = opt && opt->die_aware == 1;
   if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks))
     return fail(DASH_ERR_UNSUPPORTED, "die_aware applies to shift and symmetric shift, without fill or a supplied table");
+  const int want_cluster = opt ? opt->cluster_size : 0;
+  if (want_cluster < 0 || want_cluster > 16 || (want_cluster & (want_cluster - 1)))
+    return fail(DASH_ERR_INVALID_ARG, "cluster_size must be 0 (auto), 1, 2, 4, 8 or 16");
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -433,6 +438,45 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       (e = ensure_status(w)) != cudaSuccess)
     return fail(DASH_ERR_NO_MEMORY, "workspace allocation failed: %s", cudaGetErrorString(e));
 
+  // ---- cluster hand-offs: ranks whose predecessor runs in the same cluster
+  // take their turn from a counter in shared memory (same ranks, same bits)
+  int cluster = 1;
+  const int32_t *dev_links = nullptr;
+  if (sched_ent && mode != DASH_SCHED_ATOMIC && !die_aware && want_cluster > 1) {
+    auto fit = sched_ent->cluster_for.find({D, T});
+    if (fit == sched_ent->cluster_for.end())
+      fit = sched_ent->cluster_for.emplace(std::make_pair(D, T), dash::bwd_main_cluster_size(D, T, P)).first;
+    if (P % want_cluster != 0 || want_cluster > fit->second)
+      return fail(DASH_ERR_UNSUPPORTED, "clusters of %d do not fit the %d CTAs of this schedule", want_cluster, P);
+    const int cl = want_cluster;
+    // the device words hold a rank in 16 bits beside the links
+    bool ranks_fit = true;
+    for (size_t t = 3; t < sched_ent->tasks_h.size() && ranks_fit; t += 4)
+      ranks_fit = (sched_ent->tasks_h[t] & dash::kRankMask) <= dash::kLinkedRankMask;
+    if (cl > 1 && ranks_fit) {
+      auto &lk = sched_ent->linked_for[cl];
+      if (!lk) {
+        const size_t nt = sched_ent->tasks_h.size() / 4;
+        std::vector<int32_t> words(nt), table(sched_ent->tasks_h);
+        dash::cluster_links(sched_ent->tasks_h.data(), sched_ent->cta_off_h.data(), P, cl, BH, n, chains,
+                            words.data());
+        for (size_t t = 0; t < nt; ++t) {
+          const int32_t w = table[4 * t + 3];
+          table[4 * t + 3] = (w & ~dash::kRankMask) | (w & dash::kLinkedRankMask) | words[t];
+        }
+        std::unique_ptr<DevBuf> buf(new DevBuf());
+        if ((e = buf->reserve(std::max<size_t>(table.size(), 4) * 4)) != cudaSuccess ||
+            (e = cudaMemcpy(buf->ptr, table.data(), table.size() * 4, cudaMemcpyHostToDevice)) != cudaSuccess) {
+          sched_ent->linked_for.erase(cl);
+          return cuda_fail(e, "cluster links");
+        }
+        lk = std::move(buf);
+      }
+      cluster = cl;
+      dev_links = (const int32_t *)lk->ptr;
+    }
+  }
+
   // ---- die-aware placement: each gang on one die, its semaphores homed there
   PlacementEntry *placed = nullptr;
   if (die_aware) {
@@ -518,6 +562,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   mp.chains = chains;
   mp.chain_stride = accum_floats;
   mp.trace = opt ? reinterpret_cast<long long *>(opt->trace) : nullptr;
+  if (dev_links) {  // the task table with the links merged into its words
+    mp.tasks = (const int4 *)dev_links;
+    mp.linked = 1;
+  }
   if (placed) {
     mp.slot_of_smid = (const int *)placed->slot_of_smid.ptr;
     mp.n_smid = placed->n_smid;
@@ -526,7 +574,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (opt && opt->main_begin_event && (e = cudaEventRecord((cudaEvent_t)opt->main_begin_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
   // die-aware: one CTA per SM, each running the slot of its SM
-  if ((e = dash::launch_bwd_main(D, T, maps, mp, placed ? sms : P, stream)) != cudaSuccess)
+  if ((e = dash::launch_bwd_main(D, T, maps, mp, placed ? sms : P, stream, cluster)) != cudaSuccess)
     return cuda_fail(e, "main launch");
   if (opt && opt->main_end_event && (e = cudaEventRecord((cudaEvent_t)opt->main_end_event, stream)) != cudaSuccess)
     return cuda_fail(e, "cudaEventRecord");
@@ -781,6 +829,16 @@ dash_status_t dash_place_schedule(const int32_t *tasks, const int32_t *cta_off, 
   if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
   std::copy(plc.slot_of_smid.begin(), plc.slot_of_smid.end(), slot_of_smid_out);
   std::copy(plc.sem_idx.begin(), plc.sem_idx.end(), sem_idx_out);
+  return DASH_OK;
+}
+
+dash_status_t dash_cluster_links(const int32_t *tasks, const int32_t *cta_off, int P, int C, int BH, int n,
+                                 int chains, int32_t *links_out, long long *n_links_out) {
+  if (!tasks || !cta_off || !links_out || P < 1 || C < 1 || C > dash::kMaxClusterLinks || BH < 1 || n < 1 ||
+      chains < 1 || chains > 2)
+    return fail(DASH_ERR_INVALID_ARG, "dash_cluster_links: null pointer or size out of range");
+  const long long k = dash::cluster_links(tasks, cta_off, P, C, BH, n, chains, links_out);
+  if (n_links_out) *n_links_out = k;
   return DASH_OK;
 }
 

@@ -109,7 +109,9 @@ struct BwdCfg {
   static constexpr uint32_t oBAR = oDELTA + kStages * T * 4;
   static constexpr int kNumBars = 12 + 4 * kStages;
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = oMISC + 16;
+  static constexpr uint32_t oTURN = oMISC + 16;                  // hand-off counters, one per CTA of the cluster
+  static constexpr uint32_t oSEEN = oTURN + 4 * kMaxClusterLinks;  // turns taken from each, by the leader
+  static constexpr uint32_t kSmemBytes = oSEEN + 4 * kMaxClusterLinks;
   // tensor-memory columns
   static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
   static constexpr uint32_t cDQ = (D == 128) ? 128u : 384u;
@@ -176,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *qemptyDO = bars + bQFull0 + 3 * C::kStages; // dO buffer (+ staged dQ half) + delta free
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
+  uint32_t *turn_count = reinterpret_cast<uint32_t *>(smem + C::oTURN);
+  uint32_t *turns_seen = reinterpret_cast<uint32_t *>(smem + C::oSEEN);
 
   if ((smem_u32(smem) & 1023u) != 0) {  // swizzled operand tiles need 1024-byte alignment
     if (threadIdx.x == 0) atomicCAS(p.status, 0, kStatusSmemMisaligned);
@@ -201,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qemptyDO[s], kNumSoftWarps + 1);   // the softmax warps (delta) + the dQ half's TMA read
     }
     *abort_flag = 0;
+    for (int i = 0; i < kMaxClusterLinks; ++i) turn_count[i] = turns_seen[i] = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -215,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.linked) cluster_sync_all();  // every CTA's hand-off counters are zero before any is raised
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Guard g{abort_flag, p.status, (uint64_t)p.spin_limit_ns};
@@ -557,7 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = t_begin; t < t_end; ++t) {
       const int4 tk = nxt;
       if (t + 1 < t_end) nxt = tasks[t + 1];
-      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & kTaskRankMask;
+      // with cluster hand-offs the task word carries the links above a 16-bit rank
+      const int bh = tk.x, kv = tk.y, q = tk.z, rank = tk.w & (p.linked ? kLinkedRankMask : kTaskRankMask);
+      const int link = p.linked ? tk.w : 0;
       const bool last = tk.w & kTaskLastFlag;
       // -------- dQ partial: TMEM -> registers; tensor memory is free at once.
       mbar_wait(&bars[bDqFull], dq_phase, g);
@@ -604,10 +612,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t t0 = globaltimer_ns();
         // the time limit is checked every 64 polls: a timer read per poll
         // would stretch the gap between two polls
-        for (uint32_t it = 1; ld_acquire_gpu(sem) != pos; ++it) {
-          if ((it & 63) == 0 && globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
-            guard_fail(g, kStatusSemTimeout);
-            break;
+        if (link & kLinkTurn) {  // the predecessor runs in this cluster: its counter here
+          const int from = (link >> kLinkFromShift) & 0xF;
+          const uint32_t want = ++turns_seen[from];
+          for (uint32_t it = 1; ld_acquire_cluster_u32(turn_count + from) < want; ++it) {
+            if ((it & 63) == 0 && globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+              guard_fail(g, kStatusSemTimeout);
+              break;
+            }
+          }
+        } else {
+          for (uint32_t it = 1; ld_acquire_gpu(sem) != pos; ++it) {
+            if ((it & 63) == 0 && globaltimer_ns() - t0 > (uint64_t)p.spin_limit_ns) {
+              guard_fail(g, kStatusSemTimeout);
+              break;
+            }
           }
         }
       }
@@ -679,7 +698,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The release is cumulative: it covers the other threads' reductions,
         // which the named barrier ordered before it.  Its fence waits until L2
         // has them, so the next rank's adds land after these.
-        if (leader && !*g.abort) st_release_gpu(sem, pos + 1);
+        if (leader && !*g.abort) {
+          if (link & kLinkRelease) {
+            // the successor runs in this cluster: one fence releases both its
+            // counter for this CTA and the semaphore
+            fence_acq_rel_gpu();
+            red_relaxed_cluster_u32(mapa_rank(turn_count + cluster_rank(), (link >> kLinkToShift) & 0xF), 1u);
+            st_relaxed_gpu(sem, pos + 1);
+          } else {
+            st_release_gpu(sem, pos + 1);
+          }
+        }
       } else if (kTrace && leader) {
         trace_put<kTrace>(p, t, kTrRel0, (long long)globaltimer_ns());
       }
@@ -728,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.linked) cluster_sync_all();  // no CTA leaves while a peer may still raise its counters
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -850,7 +880,8 @@ __global__ void __launch_bounds__(256) dash_bwd_convert(const float *__restrict_
 }
 
 template <int D, int T, bool kTrace>
-cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_ctas, cudaStream_t stream) {
+cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_ctas, cudaStream_t stream,
+                          int cluster) {
   using C = BwdCfg<D, T>;
   auto kfn = dash_bwd_main<D, T, kTrace>;
   // The setmaxnreg split above assumes the CTA is launched with exactly
@@ -867,12 +898,54 @@ cudaError_t launch_main_t(const BwdMaps &maps, const BwdMainParams &p, int num_c
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;  // all CTAs resident: semaphore waits cannot starve
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    if (num_ctas % cluster != 0 || cluster > kMaxClusterLinks) return cudaErrorInvalidValue;
+    if (cluster > 8 && (e = cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
+                           cudaSuccess)
+      return e;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, kfn, maps.q, maps.k, maps.v, maps.dout, p);
+}
+
+template <int D, int T>
+int cluster_size_t(int num_ctas) {
+  using C = BwdCfg<D, T>;
+  auto kfn = dash_bwd_main<D, T, false>;
+  const int smem = C::kSmemBytes > (uint32_t)kMinSmemOneCtaPerSm ? (int)C::kSmemBytes : kMinSmemOneCtaPerSm;
+  if (cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+  for (int cl : {16, 8, 4, 2}) {
+    if (num_ctas % cl != 0) continue;
+    if (cl > 8 && cudaFuncSetAttribute(kfn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_ctas);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kfn, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // clear the error; try a smaller size
+      continue;
+    }
+    if ((long long)active * cl >= num_ctas) return cl;
+  }
+  return 1;
 }
 
 }  // namespace
@@ -899,17 +972,25 @@ cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream
 }
 
 cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int cluster) {
   if (p.trace) {  // the traced kernel exists for the 128-row tiles only
-    if (D == 64 && T == 128) return launch_main_t<64, 128, true>(maps, p, num_ctas, stream);
-    if (D == 128 && T == 128) return launch_main_t<128, 128, true>(maps, p, num_ctas, stream);
+    if (D == 64 && T == 128) return launch_main_t<64, 128, true>(maps, p, num_ctas, stream, cluster);
+    if (D == 128 && T == 128) return launch_main_t<128, 128, true>(maps, p, num_ctas, stream, cluster);
     return cudaErrorNotSupported;
   }
-  if (D == 64 && T == 64) return launch_main_t<64, 64, false>(maps, p, num_ctas, stream);
-  if (D == 64 && T == 128) return launch_main_t<64, 128, false>(maps, p, num_ctas, stream);
-  if (D == 128 && T == 64) return launch_main_t<128, 64, false>(maps, p, num_ctas, stream);
-  if (D == 128 && T == 128) return launch_main_t<128, 128, false>(maps, p, num_ctas, stream);
+  if (D == 64 && T == 64) return launch_main_t<64, 64, false>(maps, p, num_ctas, stream, cluster);
+  if (D == 64 && T == 128) return launch_main_t<64, 128, false>(maps, p, num_ctas, stream, cluster);
+  if (D == 128 && T == 64) return launch_main_t<128, 64, false>(maps, p, num_ctas, stream, cluster);
+  if (D == 128 && T == 128) return launch_main_t<128, 128, false>(maps, p, num_ctas, stream, cluster);
   return cudaErrorInvalidValue;
+}
+
+int bwd_main_cluster_size(int D, int T, int num_ctas) {
+  if (D == 64 && T == 64) return cluster_size_t<64, 64>(num_ctas);
+  if (D == 64 && T == 128) return cluster_size_t<64, 128>(num_ctas);
+  if (D == 128 && T == 64) return cluster_size_t<128, 64>(num_ctas);
+  if (D == 128 && T == 128) return cluster_size_t<128, 128>(num_ctas);
+  return 1;
 }
 
 cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,

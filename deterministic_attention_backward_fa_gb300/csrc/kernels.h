@@ -57,7 +57,19 @@ struct BwdMainParams {
   const int *slot_of_smid = nullptr;
   int n_smid = 0;
   const int *sem_idx = nullptr;
+  // Cluster hand-offs (with a cluster launch): the task words carry the links
+  // of cluster_links (schedule.h) above a 16-bit rank; a linked rank takes its
+  // turn from a counter in its own shared memory that the predecessor's CTA
+  // raises.
+  int linked = 0;
 };
+constexpr int kMaxClusterLinks = 16;  // cluster sizes up to 16: one counter per CTA of the cluster
+// Link bits of a task word (host cluster_links and the device table of a linked launch)
+constexpr int32_t kLinkedRankMask = 0xFFFF;           // ranks below 2^16 leave room for the links
+constexpr int kLinkFromShift = 16;                    // predecessor's rank in the cluster (4 bits)
+constexpr int kLinkToShift = 20;                      // successor's rank in the cluster (4 bits)
+constexpr int32_t kLinkTurn = 1 << 30;                // the turn comes from the predecessor's counter
+constexpr int32_t kLinkRelease = (int32_t)(1u << 31);  // the release also raises the successor's counter
 
 // Phase stamps of the traced main kernel, one row of kTraceSlots int64 per
 // task (indexed by the task's position in the table).  "clk" stamps are the
@@ -107,8 +119,13 @@ struct FwdParams {
 
 size_t bwd_main_smem_bytes(int D, int T);
 cudaError_t launch_bwd_preprocess(const BwdPreParams &a, int num_sms, cudaStream_t stream);
+// cluster = 1: plain cooperative launch; 2..16: thread-block clusters of that
+// size (then p.linked may be set).
 cudaError_t launch_bwd_main(int D, int T, const BwdMaps &maps, const BwdMainParams &p, int num_ctas,
-                            cudaStream_t stream);
+                            cudaStream_t stream, int cluster = 1);
+// The largest cluster size among 16, 8, 4, 2 that divides num_ctas and lets
+// every CTA of the launch be resident at once; 1 if none.
+int bwd_main_cluster_size(int D, int T, int num_ctas);
 cudaError_t launch_bwd_convert(int D, int T, const float *acc, int chains, long long chain_stride, void *dq,
                                float *acc_out, float scale, int BH,
                                int S, int n, int num_sms, cudaStream_t stream);

@@ -32,6 +32,7 @@
 #include "schedule.h"
 
 #include <algorithm>
+#include <map>
 #include <string>
 #include <cmath>
 #include <functional>
@@ -432,6 +433,50 @@ std::string check_table_order(const int32_t *tasks, const int32_t *cta_off, int 
   }
   if (finished != P) return "the table's dQ orders wait on one another in a cycle: it would never finish";
   return "";
+}
+
+long long cluster_links(const int32_t *tasks, const int32_t *cta_off, int P, int C, int BH, int n, int chains,
+                        int32_t *links_out) {
+  const int total = cta_off[P];
+  std::fill(links_out, links_out + total, 0);
+  if (C < 2 || C > kMaxClusterLinks || chains < 1) return 0;
+  std::vector<int> cta_of(total);
+  for (int c = 0; c < P; ++c)
+    for (int t = cta_off[c]; t < cta_off[c + 1]; ++t) cta_of[t] = c;
+  // tasks of each (head, tile, chain) in their order of adds
+  const size_t keys = (size_t)BH * n * chains;
+  std::vector<std::vector<std::pair<int, int>>> order(keys);  // (position, task)
+  for (int t = 0; t < total; ++t) {
+    const int32_t *k = tasks + 4 * (size_t)t;
+    const int rank = k[3] & kRankMask;
+    const size_t key = ((size_t)k[0] * n + k[2]) * chains + rank % chains;
+    if (key < keys) order[key].push_back({rank / chains, t});
+  }
+  // candidate hand-offs inside a cluster, grouped by (producer CTA, consumer CTA)
+  std::map<std::pair<int, int>, std::vector<std::pair<int, int>>> pairs;  // -> (consumer task, producer task)
+  for (auto &v : order) {
+    std::sort(v.begin(), v.end());
+    for (size_t i = 0; i + 1 < v.size(); ++i) {
+      const int tp = v[i].second, tc = v[i + 1].second;
+      const int a = cta_of[tp], b = cta_of[tc];
+      if (a / C == b / C) pairs[{a, b}].push_back({tc, tp});
+    }
+  }
+  long long linked = 0;
+  for (auto &kv : pairs) {
+    auto &lst = kv.second;
+    std::sort(lst.begin(), lst.end());  // the consumer takes its turns in task order
+    bool monotone = true;               // ... and the producer must release them in that order
+    for (size_t i = 1; i < lst.size() && monotone; ++i) monotone = lst[i].second > lst[i - 1].second;
+    if (!monotone) continue;
+    const int a = kv.first.first, b = kv.first.second;
+    for (auto &l : lst) {
+      links_out[l.second] |= kLinkRelease | ((b % C) << kLinkToShift);
+      links_out[l.first] |= kLinkTurn | ((a % C) << kLinkFromShift);
+      ++linked;
+    }
+  }
+  return linked;
 }
 
 std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, double serial_ms, int *c, int *r) {

@@ -6,6 +6,8 @@
 #include <string>
 #include <vector>
 
+#include "kernels.h"  // kLinkRelease, kLinkTurn
+
 namespace dash {
 
 enum Mode { kAtomic = 0, kSerial = 1, kDescendingQ = 2, kShift = 3, kSymmetricShift = 4 };
@@ -61,6 +63,22 @@ std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, i
 // end (no cycle of waits).  Bounds and run structure are checked elsewhere.
 // Empty string when the table is sound, else the reason.
 std::string check_table_order(const int32_t *tasks, const int32_t *cta_off, int P, int BH, int n, int chains);
+
+// Cluster links of an ordered table (an extension of the semaphore hand-off):
+// with the persistent CTAs launched in thread-block clusters of C (<= 16), a
+// rank whose successor in its dQ tile's order runs in the same cluster can
+// also signal it through that CTA's shared memory.  links_out[t] holds the
+// bits to merge into task t's word (kernels.h):
+//   kLinkRelease | (rank of the successor's CTA in the cluster << kLinkToShift):
+//     task t raises the successor's counter for t's CTA after its release;
+//   kLinkTurn | (rank of the predecessor's CTA in the cluster << kLinkFromShift):
+//     task t takes its turn from that counter instead of the global semaphore.
+// A pair of CTAs (producer a, consumer b) is linked only if b takes its turns
+// from a in the order in which a releases them, so that one counter per
+// producer suffices; otherwise both keep the global semaphore.  Returns the
+// number of linked hand-offs.
+long long cluster_links(const int32_t *tasks, const int32_t *cta_off, int P, int C, int BH, int n, int chains,
+                        int32_t *links_out);
 
 // Task costs fitted to measured times: c is fixed at kFitCostC and r is the
 // value of kFitCostR whose simulated serial / atomic makespan ratio (both on

@@ -286,6 +286,26 @@ __device__ __forceinline__ void mbar_drain_cluster(uint64_t *b, uint32_t parity,
   }
 }
 
+// Counter hand-offs inside a cluster.  The releasing thread issues one
+// fence.acq_rel at gpu scope and then two relaxed writes: the global
+// semaphore (gpu scope) and a counter in another CTA's shared memory (cluster
+// scope); a fence followed by a strong write is a release of that write, so
+// one fence serves both.  The waiting thread reads its own counter with
+// acquire at cluster scope, so what the releasing CTA wrote before the fence
+// is ordered before what the waiting CTA writes after its read.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void st_relaxed_gpu(int *p, int v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cluster_u32(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cluster.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn: 0 = K-major operand, 1 = MN-major operand.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

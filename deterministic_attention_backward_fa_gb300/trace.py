@@ -49,11 +49,11 @@ def task_table(BH, n, causal, schedule, sms, fill=False, chains=1):
 
 
 def run(q, k, v, o, do, lse, causal, scale, schedule, tasks, off, tile=128, chains=1, steps=5, warmup=3,
-        die_aware=0):
+        die_aware=0, cluster_size=0, supply_table=False):
     """Times the main kernel plain and traced on the same table; returns (trace int64 [n_tasks,
-    TRACE_SLOTS] of the last traced run, plain ms, traced ms, outputs equal).  The table is supplied,
-    except with die-aware placement, which places the library's own table (the same one task_table
-    builds)."""
+    TRACE_SLOTS] of the last traced run, plain ms, traced ms, outputs equal).  The kernel runs the
+    library's own table, which task_table reproduces (with its cluster hand-offs, or die-aware
+    placement); supply_table passes `tasks` instead (then without either)."""
     dev = q.device
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -68,10 +68,10 @@ def run(q, k, v, o, do, lse, causal, scale, schedule, tasks, off, tile=128, chai
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)   # creates the events, whose handles the library records into
             b.record(stream)
-            table = {} if die_aware else {"tasks": tasks, "cta_off": off}
+            table = {"tasks": tasks, "cta_off": off} if supply_table else {}
             dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal, scale, schedule, tile=tile,
                              main_events=(a, b), dq_chains=chains, trace=tr if traced else None,
-                             die_aware=die_aware, **table)
+                             die_aware=die_aware, cluster_size=cluster_size, **table)
             b.synchronize()
             if i >= warmup:
                 times.append(a.elapsed_time(b))
@@ -157,6 +157,8 @@ def main(argv=None):
     ap.add_argument("--fill", action="store_true")
     ap.add_argument("--chains", type=int, default=1)
     ap.add_argument("--die-aware", action="store_true", help="die-aware placement (shift schedules)")
+    ap.add_argument("--cluster-size", type=int, default=0,
+                    help="thread-block clusters of the dQ hand-offs: 0 or 1 = none, else the size")
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--out", default="")
     args = ap.parse_args(argv)
@@ -172,10 +174,12 @@ def main(argv=None):
     BH, n = w.B * w.H, w.n_blocks
     tasks, off, P = task_table(BH, n, w.causal, args.schedule, sms, args.fill, args.chains)
     tr, plain_ms, traced_ms, same = run(q, k, v, o, do, lse, w.causal, w.scale, args.schedule, tasks, off,
-                                        w.tile, args.chains, args.steps, die_aware=int(args.die_aware))
+                                        w.tile, args.chains, args.steps, die_aware=int(args.die_aware),
+                                        cluster_size=args.cluster_size)
     rows, sm_mhz, viol, n_sms = summarize(tasks, off, tr, args.chains if args.schedule != "atomic" else 0)
     name = args.schedule + (" with fill" if args.fill else "") + (" two dQ chains" if args.chains == 2 else "")
     name += " die-aware" if args.die_aware else ""
+    name += f", clusters of {args.cluster_size}" if args.cluster_size > 1 else ""
     cmd = " ".join(["python -m deterministic_attention_backward_fa_gb300.trace"] + (argv or sys.argv[1:]))
     lines = [f"# Phase trace of dash_bwd_main: {w.name}, {name}", "",
              f"Command: `{cmd}`", "",

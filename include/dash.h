@@ -149,6 +149,15 @@ typedef struct {
                             * of a few milliseconds, and a synchronisation of the stream).  The tasks, ranks
                             * and adds are those of the plain schedule, so the results are the same bits.
                             * DASH_ERR_UNSUPPORTED when the map shows no two groups of SMs. */
+  int cluster_size;        /* ordered schedules with the library's own table: the persistent CTAs run in
+                            * thread-block clusters of this size, and a rank whose predecessor in its dQ
+                            * tile's order runs in the same cluster takes its turn from a counter in its
+                            * own shared memory, which the predecessor raises after its release (the global
+                            * semaphore is released as well).  The ranks and adds do not change, so neither
+                            * do the results.  0 or 1 = no clusters (the hand-off through the global
+                            * semaphore alone measured faster); 2, 4, 8, 16 = that size
+                            * (DASH_ERR_UNSUPPORTED if it does not divide the CTA count or the GPU cannot
+                            * hold that many clusters at once).  Not with die_aware. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
@@ -332,6 +341,22 @@ dash_status_t dash_place_schedule(const int32_t *tasks, const int32_t *cta_off, 
                                   int chains, const int32_t *sm0, int n0, const int32_t *sm1, int n1,
                                   const int32_t *line0, int m0, const int32_t *line1, int m1, int max_smid,
                                   int32_t *slot_of_smid_out, int32_t *sem_idx_out);
+
+/* Cluster hand-offs of a task table (host only; the tables behind
+ * dash_bwd_options_t.cluster_size).  For a table on P CTAs launched in clusters
+ * of C, writes one word per task to links_out: bit 31 set when the task, after
+ * its release, also raises a counter of its successor in its dQ tile's order,
+ * whose CTA runs in the same cluster with rank (word >> 20) & 0xF; bit 30 set
+ * when the task takes its turn from the counter that its predecessor's CTA,
+ * of rank (word >> 16) & 0xF in the cluster, raises.  (The library merges
+ * these bits into its device copy of the task words, whose ranks then take the
+ * low 16 bits.)  A (producer, consumer) pair of
+ * CTAs is linked only when the consumer takes its turns from the producer in
+ * the order of the producer's releases.  *n_links_out receives the number of
+ * linked hand-offs.  DASH_ERR_INVALID_ARG for null pointers or C outside
+ * [1, 16]. */
+dash_status_t dash_cluster_links(const int32_t *tasks, const int32_t *cta_off, int P, int C, int BH, int n,
+                                 int chains, int32_t *links_out, long long *n_links_out);
 
 /* The die map of the calling thread's current device as the stream's
  * workspace measures it (the probe runs on `stream` the first time, which is
