@@ -48,7 +48,7 @@ class BwdOptions(ctypes.Structure):
                 ("trace", ctypes.c_void_p), ("die_aware", ctypes.c_int), ("cluster_size", ctypes.c_int)]
 
 # Slots of a trace row (dash_bwd_options_t.trace): see include/dash.h.
-TRACE_SLOTS = 17
+TRACE_SLOTS = 21
 
 
 _LIB = None

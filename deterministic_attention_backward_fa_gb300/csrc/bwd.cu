@@ -81,11 +81,18 @@ constexpr unsigned kRedPauseOrderedNs = 16;  // after every reduction
 constexpr unsigned kRedPauseAtomicNs = 96;   // after every third reduction
 constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
 constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
-constexpr int kRegsSoftmax = 128;     // warpgroups 1, 2 (unchanged)
 static_assert(kRegsProducer < kRegsLaunch, "warpgroup 0 must give registers up before the others take them");
-constexpr int kRegsReduce = 200;      // warpgroup 3 after setmaxnreg.inc (holds a dQ row)
-static_assert(kRegsProducer * 128 + 2 * kRegsSoftmax * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
-              "register split exceeds the CTA's allocation");
+// Warpgroups 1, 2 (softmax) and 3 (dQ reduction) after setmaxnreg.  At D = 128
+// the reduction holds a 128-float dQ row and the softmax keeps the launch
+// count.  At D = 64 the row is 64 floats and the three warpgroups take 152
+// each, enough for the softmax to load both 32-column chunks of a pass from
+// tensor memory at once (other splits made ptxas spill in one role or the other).
+template <int D> struct RegSplit {
+  static constexpr int kSoftmax = (D == 64) ? 152 : 128;
+  static constexpr int kReduce = (D == 64) ? 152 : 200;
+  static_assert(kRegsProducer * 128 + 2 * kSoftmax * 128 + kReduce * 128 <= kRegsLaunch * kThreads,
+                "register split exceeds the CTA's allocation");
+};
 
 template <int D, int T>
 struct BwdCfg {
@@ -144,14 +151,20 @@ template <bool kTrace>
 __device__ __forceinline__ void trace_put(const BwdMainParams &p, int t, int slot, long long v) {
   if constexpr (kTrace) p.trace[(size_t)t * kTraceSlots + slot] = v;
 }
-__device__ __forceinline__ long long clk() { return clock64(); }
+// The SM clock, read where it stands in the program: the volatile asm with a
+// memory clobber keeps the compiler from moving it across the waits it times.
+__device__ __forceinline__ long long clk() {
+  long long r;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(r) : : "memory");
+  return r;
+}
 __device__ __forceinline__ unsigned smid() {
   unsigned r;
   asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void regs_softmax() { regs_set<kRegsSoftmax>(); }
-__device__ __forceinline__ void regs_reduce() { regs_set<kRegsReduce>(); }
+template <int D> __device__ __forceinline__ void regs_softmax() { regs_set<RegSplit<D>::kSoftmax>(); }
+template <int D> __device__ __forceinline__ void regs_reduce() { regs_set<RegSplit<D>::kReduce>(); }
 
 template <int D, int T, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -178,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *qemptyDO = bars + bQFull0 + 3 * C::kStages; // dO buffer (+ staged dQ half) + delta free
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::oMISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::oMISC + 4);
+  uint32_t *pass_done = reinterpret_cast<uint32_t *>(smem + C::oMISC + 8);  // traced: softmax warps done, per pass
   uint32_t *turn_count = reinterpret_cast<uint32_t *>(smem + C::oTURN);
   uint32_t *turns_seen = reinterpret_cast<uint32_t *>(smem + C::oSEEN);
 
@@ -205,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qemptyDO[s], kNumSoftWarps + 1);   // the softmax warps (delta) + the dQ half's TMA read
     }
     *abort_flag = 0;
+    pass_done[0] = pass_done[1] = 0;
     for (int i = 0; i < kMaxClusterLinks; ++i) turn_count[i] = turns_seen[i] = 0;
     fence_mbar_init();
   }
@@ -243,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t *row0p = smem + (qside ? C::oLSE : C::oDELTA);
       const float *rowsrc = qside ? p.lse2 : p.delta;
       uint32_t kv_e_phase = 0;
-      uint32_t e_phase[C::kStages] = {};
+      PhaseBits e_phase;
       uint32_t f_last[C::kStages] = {};
       bool used[C::kStages] = {};
       bool kv_issued = false;
@@ -273,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (used[st]) {
           mbar_wait(&empty[st], e_phase[st], g);
-          e_phase[st] ^= 1;
+          e_phase.flip(st);
         }
         if (!*g.abort) {
           const uint32_t fill = used[st] ? (f_last[st] ^ 1) : 0;
@@ -296,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);   // dV, dK: A K-major (TMEM / smem), B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, D, 1, 1);    // dQ: MN-major A and B
       uint32_t kvf_phase = 0, dkve_phase = 0, pf_phase = 0, dsf_phase = 0, tf_phase = 0;
-      uint32_t qfq_phase[C::kStages] = {}, qfd_phase[C::kStages] = {};
+      PhaseBits qfq_phase, qfd_phase;
       int st = 0, runs = 0;
       const uint32_t sK = smem_u32(smem + C::oK), sV = smem_u32(smem + C::oV);
       const uint32_t sDS = smem_u32(smem + C::oDS);
@@ -304,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t dK_m = sw128_desc(sK, C::kKvPanel, 1024);                          // MN-major
       uint64_t dDS_m = sw128_desc(sDS, C::kDsPanel, 1024);                        // dS as A of dQ
       uint64_t dDS_k = sw128_desc(sDS, 16, 1024);                                 // dS^T as A of dK
-      bool issued = false, s_early = false;
+      bool issued = false, s_early = false, dp_early = false;
       // S^T = K Q^T into the S^T columns (M = 128 KV rows, N = T, K = D).  A
       // descriptor plus (byte offset >> 4) addresses the same tile further on.
       auto issue_s = [&](int stage) {
@@ -318,6 +333,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&bars[bSFull]);
         issued = true;
+      };
+      // dP^T = V dO^T into the dP^T columns (same shape as S^T).
+      auto issue_dp = [&](int stage) {
+        const uint64_t dDOk = sw128_desc(smem_u32(smem + C::oDO + stage * C::kQBytes), 16, 1024);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
+          const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::cDP, dV_k + off, dDOk + offq, idS, kk > 0);
+        }
+        tc_commit(&bars[bDpFull]);
       };
       int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
       for (int t = t_begin; t < t_end; ++t) {
@@ -340,27 +367,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("" : "+l"(dK_k), "+l"(dV_k), "+l"(dK_m), "+l"(dDS_m), "+l"(dDS_k));
         if (!s_early) {  // S^T of this task was not issued during the previous one
           mbar_wait(&qfullQ[st], qfq_phase[st], g);
-          qfq_phase[st] ^= 1;
+          qfq_phase.flip(st);
           if (!*g.abort) issue_s(st);
         }
-        mbar_wait(&qfullDO[st], qfd_phase[st], g);
-        qfd_phase[st] ^= 1;
-        if (C::kDqInDp && t > t_begin) {  // the previous dQ sits in the dP^T columns
-          mbar_wait(&bars[bTmemFree], tf_phase, g);
-          tf_phase ^= 1;
-        }
-        trace_put<kTrace>(p, t, kTrMmaDp, clk());
-        if (!*g.abort) {
-          tc_fence_after();
-          // dP^T = V dO^T
-          const uint64_t dDOk = sw128_desc(sDO, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * C::kKvPanel + (kk & 3) * 32) >> 4;
-            const uint32_t offq = ((kk >> 2) * C::kQPanel + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::cDP, dV_k + off, dDOk + offq, idS, kk > 0);
+        if (!dp_early) {  // dP^T of this task was not issued during the previous one
+          mbar_wait(&qfullDO[st], qfd_phase[st], g);
+          qfd_phase.flip(st);
+          if (C::kDqInDp && t > t_begin) {  // the previous dQ sits in the dP^T columns
+            mbar_wait(&bars[bTmemFree], tf_phase, g);
+            tf_phase ^= 1;
           }
-          tc_commit(&bars[bDpFull]);
+          trace_put<kTrace>(p, t, kTrMmaDp, clk());
+          if (!*g.abort) issue_dp(st);
         }
         mbar_wait(&bars[bPFull], pf_phase, g);
         pf_phase ^= 1;
@@ -389,13 +407,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (t + 1 < t_end && !(nxt.w & kTaskFirstFlag) && !*g.abort) {
           const int st1 = (st + 1 == C::kStages) ? 0 : st + 1;
           if (mbar_test(&qfullQ[st1], qfq_phase[st1])) {
-            qfq_phase[st1] ^= 1;
+            qfq_phase.flip(st1);
             issue_s(st1);
             s_early = true;
           }
         }
+        trace_put<kTrace>(p, t, kTrMmaDvOut, clk());
         mbar_wait(&bars[bDsFull], dsf_phase, g);
         dsf_phase ^= 1;
+        trace_put<kTrace>(p, t, kTrMmaDsSeen, clk());
+        // With dQ in columns of its own (D = 64), the next task's dP^T may go
+        // ahead of this task's dQ and dK once pass B has read this dP^T, if it
+        // stays on this KV tile and its dO tile has landed: the softmax warps
+        // then find it done when they finish the next pass A.
+        dp_early = false;
+        if (!C::kDqInDp && t + 1 < t_end && !(nxt.w & kTaskFirstFlag) && !*g.abort) {
+          const int st1 = (st + 1 == C::kStages) ? 0 : st + 1;
+          if (mbar_test(&qfullDO[st1], qfd_phase[st1])) {
+            qfd_phase.flip(st1);
+            trace_put<kTrace>(p, t + 1, kTrMmaDp, clk());
+            issue_dp(st1);
+            dp_early = true;
+          }
+        }
         if (!C::kDqInDp && t > t_begin) {
           mbar_wait(&bars[bTmemFree], tf_phase, g);
           tf_phase ^= 1;
@@ -434,13 +468,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kRedWarp0) {
     // ------------------------------------------------------------ softmax
-    regs_softmax();
+    regs_softmax<D>();
+    constexpr bool kSoftBatch = (D == 64 && C::kChunks == 2);  // both chunks of a pass in one TMEM load wait
     const int sub = warp & 3;                 // TMEM sub-partition: KV rows 32*sub ..
     const int half = (warp - kSoftWarp0) >> 2;
     const int L = sub * 32 + lane;            // this thread's KV row (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     uint32_t sf_phase = 0, dpf_phase = 0, kd_phase = 0;
-    uint32_t qfq_phase[C::kStages] = {}, qfd_phase[C::kStages] = {};
+    PhaseBits qfq_phase, qfd_phase;
     int st = 0;
     uint8_t *sDS = smem + C::oDS;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
@@ -451,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *sL = reinterpret_cast<const float *>(smem + C::oLSE + st * T * 4);
       const float *sDl = reinterpret_cast<const float *>(smem + C::oDELTA + st * T * 4);
       mbar_wait(&qfullQ[st], qfq_phase[st], g);  // LSE
-      qfq_phase[st] ^= 1;
+      qfq_phase.flip(st);
       mbar_wait(&bars[bSFull], sf_phase, g);
       sf_phase ^= 1;
       const bool tracer = kTrace && warp == kSoftWarp0 && lane == 0;
@@ -466,13 +501,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // causal mask, the tile reaches above the diagonal; the test is made
         // warp-uniform so that the unmasked path does not diverge.
         const bool masked = __any_sync(0xffffffffu, !row_ok || (p.causal && qbase < kv_g));
-        // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns
+        // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns.
+        // With the registers for it (D = 64), both chunks' S^T come in one load wait.
+        uint32_t s2[kSoftBatch ? 32 : 1];
+        if constexpr (kSoftBatch) {
+          uint32_t s0[32];
+          tmem_ld32x2(tl + C::cS + 32 * half, tl + C::cS + 32 * half + 64, s0, s2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pv[0][e] = __uint_as_float(s0[e]);
+        }
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;         // first Q column of the chunk
           const uint32_t pcol = 32 * half + 16 * c;  // its packed P column
           uint32_t s[32];
-          tmem_ld32(tl + C::cS + j0, s);
+          if constexpr (kSoftBatch) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[e] = c == 0 ? __float_as_uint(pv[0][e]) : s2[e];
+          } else {
+            tmem_ld32(tl + C::cS + j0, s);
+          }
           uint32_t pk[16];
           if (masked) {
 #pragma unroll
@@ -496,12 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (tracer) trace_put<kTrace>(p, t, kTrPassA1, clk());
+      if (kTrace && lane == 0 && (atomicAdd(pass_done, 1u) & 7u) == 7u) trace_put<kTrace>(p, t, kTrPassALast, clk());
       if (lane == 0) {
         mbar_arrive(&bars[bPFull]);
         mbar_arrive(&qemptyQ[st]);  // this warp is done with the stage's LSE
       }
       mbar_wait(&qfullDO[st], qfd_phase[st], g);  // delta
-      qfd_phase[st] ^= 1;
+      qfd_phase.flip(st);
       mbar_wait(&bars[bDpFull], dpf_phase, g);
       dpf_phase ^= 1;
       if (t > t_begin) {  // the previous task's dQ and dK MMAs have read the dS tile
@@ -513,6 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // pass B: dS = P * (dP - delta), into shared memory as [q/64][kv][64 q]:
         // the MN-major A operand of dQ = dS K and the K-major A operand of dK
+        uint32_t dpa[kSoftBatch ? 32 : 1], dpb[kSoftBatch ? 32 : 1];
+        if constexpr (kSoftBatch) tmem_ld32x2(tl + C::cDP + 32 * half, tl + C::cDP + 32 * half + 64, dpa, dpb);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;
@@ -520,7 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb) {  // 16 columns at a time keeps register use down
             uint32_t dp[16];
-            tmem_ld16(tl + C::cDP + j0 + 16 * sb, dp);
+            if constexpr (kSoftBatch) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) dp[e] = c == 0 ? dpa[16 * sb + e] : dpb[16 * sb + e];
+            } else {
+              tmem_ld16(tl + C::cDP + j0 + 16 * sb, dp);
+            }
             uint32_t dk[8];
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
@@ -542,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (tracer) trace_put<kTrace>(p, t, kTrPassB1, clk());
+      if (kTrace && lane == 0 && (atomicAdd(pass_done + 1, 1u) & 7u) == 7u) trace_put<kTrace>(p, t, kTrPassBLast, clk());
       if (lane == 0) {
         mbar_arrive(&bars[bDsFull]);
         mbar_arrive(&qemptyDO[st]);  // this warp is done with the stage's delta
@@ -550,13 +607,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ reduction + epilogue
-    regs_reduce();
+    regs_reduce<D>();
     const int sub = warp & 3;
     const int L = sub * 32 + lane;            // Q row of dQ, KV row of dK/dV
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     const bool ordered = p.ordered != 0;
     const bool leader = threadIdx.x == kRedWarp0 * 32;
     constexpr int kHalfChunks = D / 8;        // 16-byte chunks per half of a dQ row
+    // the atomic schedule's bulk half pays at D = 128 only (measured); at D = 64
+    // every schedule adds the whole partial from registers
+    constexpr bool kAtomicBulk = (D == 128);
     uint32_t dq_phase = 0, dkvf_phase = 0;
     int st = 0;
     int4 nxt = t_begin < t_end ? tasks[t_begin] : make_int4(0, 0, 0, 0);
@@ -640,8 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // vector reductions, and adds the first half from registers meanwhile.
       if (kTrace && leader) trace_put<kTrace>(p, t, kTrAcq1, (long long)globaltimer_ns());
       named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
-      const int red_vecs = ordered ? 2 * kHalfChunks : kHalfChunks;
-      if (ordered) {
+      const bool all_regs = ordered || !kAtomicBulk;
+      const int red_vecs = all_regs ? 2 * kHalfChunks : kHalfChunks;
+      if (all_regs) {
         if (leader) mbar_arrive(&qemptyDO[st]);  // the dO buffer is not used for dQ
       } else {
         uint8_t *stage = smem + C::oDO + st * C::kQBytes;
@@ -683,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c < red_vecs) {
               red_add_v4(row + (size_t)c * T * 4, acc[4 * c], acc[4 * c + 1], acc[4 * c + 2], acc[4 * c + 3]);
               if (c + 1 < red_vecs) {
-                if (ordered)
+                if (all_regs)
                   __nanosleep(kRedPauseOrderedNs);
                 else if (c % 3 == 2)
                   __nanosleep(kRedPauseAtomicNs);

@@ -92,7 +92,11 @@ enum TraceSlot {
   kTrClkAtAcq0 = 14, // clk read next to kTrAcq0, to put both clocks on one axis
   kTrMeta = 15,      // smid * 65536 + the CTA's slot (its task list)
   kTrRel1 = 16,      // ns: the release store has returned (its fence is done)
-  kTraceSlots = 17
+  kTrPassALast = 17, // clk: the last of the eight softmax warps is done with pass A
+  kTrPassBLast = 18, // clk: the last of the eight softmax warps is done with pass B
+  kTrMmaDvOut = 19,  // clk: MMA warp has issued dV (and the next S^T, when it goes early)
+  kTrMmaDsSeen = 20, // clk: MMA warp's wait for dS has returned
+  kTraceSlots = 21
 };
 
 struct BwdPreParams {

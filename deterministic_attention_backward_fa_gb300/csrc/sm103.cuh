@@ -59,6 +59,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t *b, uint32_t parity) {
   return ok != 0;
 }
 
+// Phases of a ring of mbarriers, one bit per stage in one register (an array
+// indexed by a run-time stage would live in local memory).
+struct PhaseBits {
+  uint32_t v = 0;
+  __device__ __forceinline__ uint32_t operator[](int s) const { return (v >> s) & 1u; }
+  __device__ __forceinline__ void flip(int s) { v ^= 1u << s; }
+};
+
 // Shared abort state of one CTA: a wait that runs out sets `abort` and the
 // device status word; from then on every wait of the CTA returns at once and
 // the roles skip their work while keeping the same control flow.

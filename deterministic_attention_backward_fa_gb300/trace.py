@@ -31,6 +31,7 @@ from . import (TRACE_SLOTS, attn_fwd, dash_attn_bwd_ex, dash_build_schedule, das
 MMA_DP, MMA_DV, MMA_DQ, MMA_END = 0, 1, 2, 3
 PASS_A0, PASS_A1, PASS_B0, PASS_B1 = 4, 5, 6, 7
 RED_Q, RED_LD, ACQ0, ACQ1, RED_ISSUED, REL0, CLK_AT_ACQ0, META, REL1 = 8, 9, 10, 11, 12, 13, 14, 15, 16
+PASS_A_LAST, PASS_B_LAST, MMA_DV_OUT, MMA_DS_SEEN = 17, 18, 19, 20
 
 L2_FLUSH_BYTES = 256 << 20
 
@@ -119,6 +120,10 @@ def summarize(tasks, off, tr, chains=1):
     rows.append(("pass A (S^T -> P), clk", _q(d(PASS_A0, PASS_A1))))
     rows.append(("pass A end until pass B starts (dP^T landed, dS buffer free), clk", _q(d(PASS_A1, PASS_B0))))
     rows.append(("pass B (dP^T -> dS), clk", _q(d(PASS_B0, PASS_B1))))
+    rows.append(("pass A: softmax warp 4 done until the last softmax warp is done, clk", _q(d(PASS_A1, PASS_A_LAST))))
+    rows.append(("pass B: softmax warp 4 done until the last softmax warp is done, clk", _q(d(PASS_B1, PASS_B_LAST))))
+    rows.append(("pass B end until the next pass A starts (next S^T done, its LSE landed), clk",
+                 _q(tr[nxt + 1, PASS_A0] - tr[nxt, PASS_B1])))
     rows.append(("dQ MMA issued until the partial is in registers, clk", _q(d(MMA_DQ, RED_LD))))
     rows.append(("reduction warps: wait for the tile's turn, ns", _q(d(ACQ0, ACQ1))))
     rows.append(("reduction warps: turn taken until every add is issued, ns", _q(d(ACQ1, REL0))))

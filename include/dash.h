@@ -173,9 +173,13 @@ typedef struct {
  * 14 clk read next to slot 10 (puts the two clocks on one axis)
  * 15 smid * 65536 + the CTA's slot (its task list)
  * 16 ns  the release store has returned (its fence is done)
- * (softmax stamps come from softmax warp 4, reduction stamps from the reduction leader;
+ * 17 clk the last of the eight softmax warps is done with pass A
+ * 18 clk the last of the eight softmax warps is done with pass B
+ * 19 clk MMA warp has issued dV (and the next S^T when it goes early)
+ * 20 clk MMA warp's wait for dS has returned
+ * (slots 4-7 come from softmax warp 4, reduction stamps from the reduction leader;
  * for the atomic schedule slots 10, 11 and 13 carry no wait) */
-#define DASH_TRACE_SLOTS 17
+#define DASH_TRACE_SLOTS 21
 
 /* dash_attn_bwd with options (opt may be NULL).  A supplied task table is
  * checked on the host before the launch: indices in range, runs on one KV tile

@@ -41,7 +41,8 @@ def test_trace_stamps_every_task_in_order(S, D, causal, sched, chains):
                    T.REL1]] > 0).all(), "a task was not stamped"
     for a, b in ((T.MMA_DP, T.MMA_DV), (T.MMA_DV, T.MMA_DQ), (T.MMA_DQ, T.MMA_END), (T.PASS_A0, T.PASS_A1),
                  (T.PASS_A1, T.PASS_B0), (T.PASS_B0, T.PASS_B1), (T.RED_Q, T.RED_LD), (T.ACQ0, T.ACQ1),
-                 (T.ACQ1, T.REL0), (T.REL0, T.REL1)):
+                 (T.ACQ1, T.REL0), (T.REL0, T.REL1), (T.PASS_A1, T.PASS_A_LAST), (T.PASS_B1, T.PASS_B_LAST),
+                 (T.PASS_A_LAST, T.MMA_DV)):
         assert (tr[:, b] >= tr[:, a]).all(), f"slot {b} stamped before slot {a}"
     ctas_seen = {int(x) & 0xFFFF for x in tr[:, T.META]}
     assert ctas_seen == {c for c in range(ctas) if off[c + 1] > off[c]}
