@@ -82,17 +82,10 @@ constexpr unsigned kRedPauseAtomicNs = 96;   // after every third reduction
 constexpr int kRegsLaunch = 128;      // 512 threads x 128 = the whole register file
 constexpr int kRegsProducer = 56;     // warpgroup 0 after setmaxnreg.dec
 static_assert(kRegsProducer < kRegsLaunch, "warpgroup 0 must give registers up before the others take them");
-// Warpgroups 1, 2 (softmax) and 3 (dQ reduction) after setmaxnreg.  At D = 128
-// the reduction holds a 128-float dQ row and the softmax keeps the launch
-// count.  At D = 64 the row is 64 floats and the three warpgroups take 152
-// each, enough for the softmax to load both 32-column chunks of a pass from
-// tensor memory at once (other splits made ptxas spill in one role or the other).
-template <int D> struct RegSplit {
-  static constexpr int kSoftmax = (D == 64) ? 152 : 128;
-  static constexpr int kReduce = (D == 64) ? 152 : 200;
-  static_assert(kRegsProducer * 128 + 2 * kSoftmax * 128 + kReduce * 128 <= kRegsLaunch * kThreads,
-                "register split exceeds the CTA's allocation");
-};
+constexpr int kRegsSoftmax = 128;     // warpgroups 1, 2 (unchanged)
+constexpr int kRegsReduce = 200;      // warpgroup 3 after setmaxnreg.inc (holds a dQ row)
+static_assert(kRegsProducer * 128 + 2 * kRegsSoftmax * 128 + kRegsReduce * 128 <= kRegsLaunch * kThreads,
+              "register split exceeds the CTA's allocation");
 
 template <int D, int T>
 struct BwdCfg {
@@ -163,8 +156,8 @@ __device__ __forceinline__ unsigned smid() {
   asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
   return r;
 }
-template <int D> __device__ __forceinline__ void regs_softmax() { regs_set<RegSplit<D>::kSoftmax>(); }
-template <int D> __device__ __forceinline__ void regs_reduce() { regs_set<RegSplit<D>::kReduce>(); }
+__device__ __forceinline__ void regs_softmax() { regs_set<kRegsSoftmax>(); }
+__device__ __forceinline__ void regs_reduce() { regs_set<kRegsReduce>(); }
 
 template <int D, int T, bool kTrace>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -468,8 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kRedWarp0) {
     // ------------------------------------------------------------ softmax
-    regs_softmax<D>();
-    constexpr bool kSoftBatch = (D == 64 && C::kChunks == 2);  // both chunks of a pass in one TMEM load wait
+    regs_softmax();
     const int sub = warp & 3;                 // TMEM sub-partition: KV rows 32*sub ..
     const int half = (warp - kSoftWarp0) >> 2;
     const int L = sub * 32 + lane;            // this thread's KV row (TMEM lane)
@@ -501,26 +493,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // causal mask, the tile reaches above the diagonal; the test is made
         // warp-uniform so that the unmasked path does not diverge.
         const bool masked = __any_sync(0xffffffffu, !row_ok || (p.causal && qbase < kv_g));
-        // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns.
-        // With the registers for it (D = 64), both chunks' S^T come in one load wait.
-        uint32_t s2[kSoftBatch ? 32 : 1];
-        if constexpr (kSoftBatch) {
-          uint32_t s0[32];
-          tmem_ld32x2(tl + C::cS + 32 * half, tl + C::cS + 32 * half + 64, s0, s2);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pv[0][e] = __uint_as_float(s0[e]);
-        }
+        // pass A: P = exp(scale * S - LSE) (masked), packed bf16 into the S^T columns
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;         // first Q column of the chunk
           const uint32_t pcol = 32 * half + 16 * c;  // its packed P column
           uint32_t s[32];
-          if constexpr (kSoftBatch) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[e] = c == 0 ? __float_as_uint(pv[0][e]) : s2[e];
-          } else {
-            tmem_ld32(tl + C::cS + j0, s);
-          }
+          tmem_ld32(tl + C::cS + j0, s);
           uint32_t pk[16];
           if (masked) {
 #pragma unroll
@@ -562,8 +541,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // pass B: dS = P * (dP - delta), into shared memory as [q/64][kv][64 q]:
         // the MN-major A operand of dQ = dS K and the K-major A operand of dK
-        uint32_t dpa[kSoftBatch ? 32 : 1], dpb[kSoftBatch ? 32 : 1];
-        if constexpr (kSoftBatch) tmem_ld32x2(tl + C::cDP + 32 * half, tl + C::cDP + 32 * half + 64, dpa, dpb);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
           const int j0 = 32 * half + 64 * c;
@@ -571,12 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int sb = 0; sb < 2; ++sb) {  // 16 columns at a time keeps register use down
             uint32_t dp[16];
-            if constexpr (kSoftBatch) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) dp[e] = c == 0 ? dpa[16 * sb + e] : dpb[16 * sb + e];
-            } else {
-              tmem_ld16(tl + C::cDP + j0 + 16 * sb, dp);
-            }
+            tmem_ld16(tl + C::cDP + j0 + 16 * sb, dp);
             uint32_t dk[8];
 #pragma unroll
             for (int e = 0; e < 16; e += 2) {
@@ -607,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ reduction + epilogue
-    regs_reduce<D>();
+    regs_reduce();
     const int sub = warp & 3;
     const int L = sub * 32 + lane;            // Q row of dQ, KV row of dK/dV
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
