@@ -110,7 +110,7 @@ struct BwdCfg {
   static constexpr int kNumBars = 12 + 4 * kStages;
   static constexpr uint32_t oMISC = oBAR + kNumBars * 8;
   static constexpr uint32_t oTURN = oMISC + 16;                  // hand-off counters, one per CTA of the cluster
-  static constexpr uint32_t oSEEN = oTURN + 4 * kMaxClusterLinks;  // turns taken from each, by the leader
+  static constexpr uint32_t oSEEN = oTURN + 4 * kMaxClusterLinks;  // turns taken from each, by the poller
   static constexpr uint32_t kSmemBytes = oSEEN + 4 * kMaxClusterLinks;
   // tensor-memory columns
   static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
@@ -585,6 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(sub * 32) << 16);
     const bool ordered = p.ordered != 0;
     const bool leader = threadIdx.x == kRedWarp0 * 32;
+    // The turn of a task is awaited by a thread of the next warp: the leader
+    // may still be in the previous task's release (its fence), and the wait
+    // then overlaps it; the adds start once both are over (the named barrier).
+    const bool poller = threadIdx.x == (kRedWarp0 + 1) * 32;
     constexpr int kHalfChunks = D / 8;        // 16-byte chunks per half of a dQ row
     // the atomic schedule's bulk half pays at D = 128 only (measured); at D = 64
     // every schedule adds the whole partial from registers
@@ -636,11 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int *sem = p.sem + (p.sem_idx ? (size_t)p.sem_idx[sem_key] : sem_key * kSemStride);
       float *dst = p.dq_accum + chain * p.chain_stride + ((size_t)bh * p.n + q) * (size_t)(T * D);
       const bool first_rank = ordered && pos == 0;  // first in its chain's order: store
-      if (kTrace && leader) {
+      if (kTrace && poller) {
         trace_put<kTrace>(p, t, kTrClkAtAcq0, clk());
         trace_put<kTrace>(p, t, kTrAcq0, (long long)globaltimer_ns());
       }
-      if (leader && ordered && !*g.abort) {
+      if (poller && ordered && !*g.abort) {
         const uint64_t t0 = globaltimer_ns();
         // the time limit is checked every 64 polls: a timer read per poll
         // would stretch the gap between two polls
@@ -670,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // buffer (dV, its last reader, completed before dQ) for a bulk
       // reduce-add by the TMA engine, which moves data faster than the
       // vector reductions, and adds the first half from registers meanwhile.
-      if (kTrace && leader) trace_put<kTrace>(p, t, kTrAcq1, (long long)globaltimer_ns());
+      if (kTrace && poller) trace_put<kTrace>(p, t, kTrAcq1, (long long)globaltimer_ns());
       named_bar(kDrainBar, kRedThreads);  // the tile's turn has come
       const bool all_regs = ordered || !kAtomicBulk;
       const int red_vecs = all_regs ? 2 * kHalfChunks : kHalfChunks;
