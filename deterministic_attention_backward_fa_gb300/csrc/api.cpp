@@ -15,6 +15,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <climits>
 #include <map>
 #include <memory>
 #include <mutex>
@@ -318,6 +319,9 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   const int n = (S + T - 1) / T;
   std::string why = dash::check_mode(mode, n, causal != 0);
   if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  // task tables index tasks, and the semaphore buffer its words, with 32-bit ints
+  if (dash::num_tasks(BH, n, causal != 0) > INT32_MAX || (long long)BH * n * (2 * dash::kSemStride + 1) > INT32_MAX)
+    return fail(DASH_ERR_UNSUPPORTED, "%lld tasks: beyond the 32-bit task tables", dash::num_tasks(BH, n, causal != 0));
   const int c = (opt && opt->cost_c > 0) ? opt->cost_c : 4;
   const int r = (opt && opt->cost_r > 0) ? opt->cost_r : 1;
   const long long spin = (opt && opt->spin_limit_ns > 0) ? opt->spin_limit_ns : kDefaultSpinNs;

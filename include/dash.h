@@ -62,7 +62,8 @@ typedef enum {
 typedef enum {
   DASH_OK = 0,
   DASH_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad scale, misaligned pointer */
-  DASH_ERR_UNSUPPORTED = 2,   /* D not 64/128, schedule invalid for the mask, odd n for symmetric shift, too few SMs */
+  DASH_ERR_UNSUPPORTED = 2,   /* D not 64/128, schedule invalid for the mask, odd n for symmetric shift, too few SMs,
+                               * or more tasks than 32-bit task tables index (2^31 - 1) */
   DASH_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message in dash_last_error) */
   DASH_ERR_TIMEOUT = 4,       /* a bounded device wait ran out (reported by dash_sync_status) */
   DASH_ERR_NO_MEMORY = 5,     /* workspace allocation failed */

@@ -111,6 +111,11 @@ def test_error_codes_without_gpu():
     opt = dash.BwdOptions(0, 0, 0, 0, 0, None, None, None, None, None, 3)
     assert L.dash_attn_bwd_ex(*([fake] * 9), 1, 1, 128, 64, 0, 0.1, 1, ctypes.byref(opt), nul) == 1
     assert "dq_chains" in dash.dash_last_error()
+    # more tasks than the 32-bit task tables index: 2^16 heads at S = 2^20 (full mask, n = 8192)
+    assert L.dash_attn_bwd(*([fake] * 9), 1, 1 << 16, 1 << 20, 64, 0, 0.1, 1, nul) == 2
+    assert "32-bit" in dash.dash_last_error()
+    # and a causal one of 2^12 heads (1.4e11 tasks)
+    assert L.dash_attn_bwd(*([fake] * 9), 1, 1 << 12, 1 << 20, 64, 1, 0.1, 1, nul) == 2
 
 
 @pytest.mark.parametrize("BH,n,causal,c,r", [(8, 4, False, 4, 1), (8, 4, False, 1, 4), (6, 8, True, 4, 1),
