@@ -591,7 +591,17 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
 }  // namespace
 
 namespace dash {
-// Lets other translation units of the library report through dash_last_error().
+// Lets other translation units of the library report through dash_last_error():
+// formats the message, keeps it for this thread and returns the code.
+dash_status_t report(dash_status_t code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
 void set_last_error(const char *msg) { g_last_error = msg; }
 // The backward's tensor maps for other translation units of the library.
 bool encode_bhsd_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows) {

@@ -35,7 +35,6 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
-#include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <map>
@@ -48,7 +47,7 @@
 #include "schedule.h"
 
 namespace dash {
-void set_last_error(const char *msg);  // api.cpp
+dash_status_t report(dash_status_t code, const char *fmt, ...);  // api.cpp: sets dash_last_error()
 // TMA map over a contiguous bf16 [BH][S][D] tensor, as the backward's kernels read it (api.cpp)
 bool encode_bhsd_map(CUtensorMap *m, const void *base, int BH, int S, int D, int box_rows);
 }
@@ -65,14 +64,9 @@ std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
 std::map<std::tuple<int, int, int, int, int, int>, dash::Schedule> g_tables;  // host copies
 
-dash_status_t fail(dash_status_t code, const char *fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  dash::set_last_error(buf);  // what dash_last_error() returns on this thread
-  return code;
+template <typename... A>
+dash_status_t fail(dash_status_t code, const char *fmt, A... args) {
+  return dash::report(code, fmt, args...);
 }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
