@@ -114,6 +114,8 @@ def summarize(tasks, off, tr, chains=1):
                  _q(tr[nxt + 1, MMA_DP] - tr[nxt, MMA_DP])))
     rows.append(("MMA warp: dP^T issued until P is ready (pass A), clk", _q(d(MMA_DP, MMA_DV))))
     rows.append(("MMA warp: dV (+ next S^T) issued until dS is ready (pass B), clk", _q(d(MMA_DV, MMA_DQ))))
+    rows.append(("  of which issuing dV (and the next S^T), clk", _q(d(MMA_DV, MMA_DV_OUT))))
+    rows.append(("  of which waiting for dS, clk", _q(d(MMA_DV_OUT, MMA_DS_SEEN))))
     rows.append(("MMA warp: dQ and dK issued, clk", _q(d(MMA_DQ, MMA_END))))
     rows.append(("MMA warp: end of task until the next dP^T (Q/dO landed, dQ drained), clk",
                  _q(tr[nxt + 1, MMA_DP] - tr[nxt, MMA_END])))
