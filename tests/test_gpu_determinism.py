@@ -148,3 +148,19 @@ def test_fill_bit_identical_across_runs(wname, sched):
         same = same and all(torch.equal(a, b) for a, b in zip(outs, first))
     dash.dash_sync_status()
     assert same, f"{wname}: {sched} with fill is not bit-identical across {RUNS} runs"
+
+
+@pytest.mark.parametrize("causal,sched", [(False, "shift"), (False, "serial"), (True, "symmetric_shift"),
+                                          (True, "descending_q")])
+def test_same_bits_whatever_the_cta_count(causal, sched):
+    # a dQ tile's rank order is fixed by the schedule (KV index or step), not by
+    # which CTA runs which chain, so every CTA count gives the same bits
+    P = Problem(2, 3, 1024, 128, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    ref = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched)
+    gang = 8 if sched == "shift" else 4 if sched == "symmetric_shift" else 1
+    for ctas in (gang, 3 * gang, 6 * gang):
+        got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, num_ctas=ctas)
+        dash.dash_sync_status()
+        for name, a, b in zip(("dQ", "dK", "dV"), got, ref):
+            assert torch.equal(a, b), f"{sched} on {ctas} CTAs: {name} differs"
