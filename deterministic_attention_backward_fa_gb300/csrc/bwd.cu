@@ -33,10 +33,13 @@
 //                ordered before the release.  No shared memory is held while
 //                the chain advances.  With two chains (an option) the tile's
 //                even and odd ranks go to two accumulators, each its own chain.
-//                For the atomic schedule, half the partial is staged in the
-//                task's dO buffer (dV has read it) and added by the TMA engine
-//                (bulk reduce-add), the other half by vector reductions.  At
-//                the end of a KV run these warps write dK and dV
+//                A lane of the second of these warps waits for the turn, so
+//                that the wait overlaps the leader's previous release.  For
+//                the atomic schedule at D = 128, half the partial is staged in
+//                the task's dO buffer (dV has read it) and added by the TMA
+//                engine (bulk reduce-add), the other half by vector
+//                reductions; at D = 64 all of it from registers.  At the end
+//                of a KV run these warps write dK and dV
 // setmaxnreg gives the reduction warpgroup enough registers to hold a dQ row.
 //
 // All MMAs are M = 128: the lanes are KV rows for S^T = K Q^T, dP^T = V dO^T,
@@ -54,7 +57,8 @@
 // D = 64.
 //
 // Per task the MMA warp issues S^T, dP^T (once the previous dQ has left the
-// dP^T columns), dV, then, if the next task stays on this KV tile and its Q
+// dP^T columns; at D = 64 one task early, right after pass B has read the
+// previous dP^T), dV, then, if the next task stays on this KV tile and its Q
 // tile has landed, the next S^T, so that pass A of the next task overlaps
 // this task's dQ and dK; then dQ and dK.
 #include <cuda_runtime.h>
