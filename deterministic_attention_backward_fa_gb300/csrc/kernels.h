@@ -85,7 +85,7 @@ enum TraceSlot {
   kTrPassB1 = 7,     // clk: pass B done
   kTrRedQ = 8,       // clk: reduction leader sees the dQ partial in tensor memory
   kTrRedLd = 9,      // clk: the partial is in registers, tensor memory released
-  kTrAcq0 = 10,      // ns: the leader starts waiting for the tile's turn
+  kTrAcq0 = 10,      // ns: the turn's waiter (a lane of the second reduction warp) starts waiting
   kTrAcq1 = 11,      // ns: the tile's turn has come (semaphore acquired; atomic: at once)
   kTrRedIssued = 12, // clk: the leader's own reductions are issued
   kTrRel0 = 13,      // ns: every reduction of the task is issued; the release of rank + 1 starts

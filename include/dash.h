@@ -178,7 +178,8 @@ typedef struct {
  * 18 clk the last of the eight softmax warps is done with pass B
  * 19 clk MMA warp has issued dV (and the next S^T when it goes early)
  * 20 clk MMA warp's wait for dS has returned
- * (slots 4-7 come from softmax warp 4, reduction stamps from the reduction leader;
+ * (slots 4-7 come from softmax warp 4; slots 10, 11 and 14 from the lane of the second
+ * reduction warp that waits for the turn, the other reduction stamps from the reduction leader;
  * for the atomic schedule slots 10, 11 and 13 carry no wait) */
 #define DASH_TRACE_SLOTS 21
 
