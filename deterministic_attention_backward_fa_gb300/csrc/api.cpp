@@ -331,6 +331,13 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1))
     return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
   const bool fill = (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT) && opt && opt->shift_fill == 1;
+  const int split = (opt && opt->shift_split > 1) ? opt->shift_split : 1;
+  if (opt && opt->shift_split < 0) return fail(DASH_ERR_INVALID_ARG, "shift_split must be >= 0");
+  if (split > 1) {
+    if (fill || (opt && opt->tasks)) return fail(DASH_ERR_UNSUPPORTED, "shift_split applies to the library's own table, without fill");
+    why = dash::check_split(mode, n, split);
+    if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  }
   if (opt && (opt->die_aware < 0 || opt->die_aware > 1)) return fail(DASH_ERR_INVALID_ARG, "die_aware must be 0 or 1");
   const bool die_aware = opt && opt->die_aware == 1;
   if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks))
@@ -378,7 +385,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   } else {
     const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
     if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
-    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains, fill ? 1 : 0);
+    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains, fill ? -1 : split);
     auto &ent = g_sched[key];
     if (!ent) {
       std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
@@ -390,7 +397,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       int Puse = want;
       if (!Puse && !fill && chains == 2 && mode == DASH_SCHED_SHIFT)
         Puse = (int)std::min<long long>(sms, (long long)BH * n);
-      if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r);
+      if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r, split);
       if (Puse < 1 && !fill) {
         g_sched.erase(key);
         return fail(DASH_ERR_UNSUPPORTED, "no CTA count up to %d SMs runs this schedule without deadlock", sms);
@@ -400,7 +407,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
         why = dash::build_fill(BH, n, causal != 0, mode, want ? want : sms, c, r, &sch, nullptr, nullptr);
         Puse = sch.P;
       } else {
-        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch);
+        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch, split);
       }
       if (!why.empty()) {
         g_sched.erase(key);
@@ -786,6 +793,27 @@ dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t s
   if (fill_schedule_out) *fill_schedule_out = fm;
   if (makespan_out) *makespan_out = s.makespan;
   return DASH_OK;
+}
+
+dash_status_t dash_build_split_schedule(int BH, int n, int causal, dash_schedule_t schedule, int split, int P,
+                                        int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
+                                        long long *makespan_out) {
+  if (!tasks_out || !cta_off_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
+  std::string why = dash::check_mode((int)schedule, n, causal != 0);
+  if (why.empty()) why = dash::check_split((int)schedule, n, split);
+  if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  dash::Schedule s;
+  why = dash::build_schedule(BH, n, causal != 0, (int)schedule, P, cost_c, cost_r, &s, split);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
+  std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
+  if (makespan_out) *makespan_out = s.makespan;
+  return DASH_OK;
+}
+
+int dash_choose_split_ctas(int BH, int n, int causal, dash_schedule_t schedule, int split, int max_ctas, int cost_c,
+                           int cost_r) {
+  return dash::choose_ctas(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r, split);
 }
 
 int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int cost_c, int cost_r) {

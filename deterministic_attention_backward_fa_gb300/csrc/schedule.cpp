@@ -49,7 +49,7 @@ struct HeadPlan {
   std::vector<int> kv, q, rank;
 };
 
-HeadPlan head_plan(int mode, int n, bool causal) {
+HeadPlan head_plan(int mode, int n, bool causal, int split = 1) {
   HeadPlan hp;
   hp.off.push_back(0);
   auto push = [&](int kv, int q) {
@@ -83,11 +83,15 @@ HeadPlan head_plan(int mode, int n, bool causal) {
   const int nt = (int)hp.kv.size();
   hp.rank.assign(nt, 0);
   if (mode == kShift || mode == kSymmetricShift) {
-    // rank = position of the visiting step among all visits of the tile
-    std::vector<std::vector<std::pair<int, int>>> visits(n);  // (step, task)
+    // rank = position of the visiting step among all visits of the tile; with
+    // split gangs, of (sub-gang, step): sub-gang s takes the tile's ranks
+    // after sub-gang s - 1 has added all of its partials
+    std::vector<std::vector<std::pair<long long, int>>> visits(n);  // (order key, task)
     const int nch = (int)hp.off.size() - 1;
+    const int g = nch / split;
     for (int c = 0; c < nch; ++c)
-      for (int t = hp.off[c]; t < hp.off[c + 1]; ++t) visits[hp.q[t]].push_back({t - hp.off[c], t});
+      for (int t = hp.off[c]; t < hp.off[c + 1]; ++t)
+        visits[hp.q[t]].push_back({(long long)(c / g) * (n + 1) + (t - hp.off[c]), t});
     for (int q = 0; q < n; ++q) {
       auto &v = visits[q];
       std::sort(v.begin(), v.end());
@@ -120,8 +124,10 @@ struct SimResult {
   std::vector<std::vector<int>> chains_of_cta;
 };
 
+// order (optional): the global chain id (head * chains per head + chain) of
+// each dispatch, in dispatch order; identity when null.
 SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, int P, int c, int r,
-                   bool ordered) {
+                   bool ordered, const std::vector<long long> *order = nullptr) {
   const int cph = (int)hp.off.size() - 1;   // chains per head
   const int tph = (int)hp.kv.size();        // tasks per head
   const long long nch = (long long)BH * cph;
@@ -148,7 +154,8 @@ SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, in
     return hp.off[lc + 1] - hp.off[lc];
   };
   auto dispatch = [&](int s, long long T) {
-    const long long ch = next++;
+    const long long ch = order ? (*order)[(size_t)next] : next;
+    ++next;
     cta_chain[s] = ch;
     cta_step[s] = 0;
     cta_phase[s] = 'C';
@@ -214,7 +221,27 @@ SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, in
   return res;
 }
 
+// Dispatch order of split gangs: every head's sub-gang 0, then every head's
+// sub-gang 1, and so on, each sub-gang's chains together.
+std::vector<long long> split_order(int BH, int cph, int split) {
+  std::vector<long long> order;
+  order.reserve((size_t)BH * cph);
+  const int g = cph / split;
+  for (int s = 0; s < split; ++s)
+    for (int h = 0; h < BH; ++h)
+      for (int k = 0; k < g; ++k) order.push_back((long long)h * cph + s * g + k);
+  return order;
+}
+
 }  // namespace
+
+std::string check_split(int mode, int n, int split) {
+  if (split <= 1) return "";
+  if (mode != kShift && mode != kSymmetricShift) return "split gangs apply to shift and symmetric shift only";
+  const int cph = chains_per_head(mode, n);
+  if (cph % split) return "the split must divide the chains of a head's gang";
+  return "";
+}
 
 std::string check_mode(int mode, int n, bool causal) {
   if (mode < kAtomic || mode > kSymmetricShift) return "unknown schedule";
@@ -233,13 +260,17 @@ long long num_tasks(int BH, int n, bool causal) {
 }
 
 std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
-                           Schedule *out) {
+                           Schedule *out, int split) {
   std::string e = check_mode(mode, n, causal);
   if (!e.empty()) return e;
+  if (split < 1) split = 1;
+  if (!(e = check_split(mode, n, split)).empty()) return e;
   if (BH < 1 || P < 1 || c < 1 || r < 1) return "BH, P and the costs must be >= 1";
-  const HeadPlan hp = head_plan(mode, n, causal);
+  const HeadPlan hp = head_plan(mode, n, causal, split);
   const std::vector<int> hpred = head_pred(hp, n);
-  SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic);
+  const std::vector<long long> order = split > 1 ? split_order(BH, (int)hp.off.size() - 1, split)
+                                                 : std::vector<long long>();
+  SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic, split > 1 ? &order : nullptr);
   if (sim.deadlock) return "schedule simulation deadlocked (too few CTAs for the chain gang?)";
   const int cph = (int)hp.off.size() - 1;
   out->tasks.clear();
@@ -266,10 +297,11 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
   return "";
 }
 
-int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
-  if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1) return -1;
+int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split) {
+  if (split < 1) split = 1;
+  if (!check_mode(mode, n, causal).empty() || !check_split(mode, n, split).empty() || BH < 1 || P_max < 1) return -1;
   const long long nch = (long long)BH * chains_per_head(mode, n);
-  const int gang = chains_per_head(mode, n);
+  const int gang = chains_per_head(mode, n) / split;  // with split gangs, a sub-gang
   // Shift makes every chain of a head wait on its neighbour in the gang, so a
   // gang split over time stalls: it only takes whole gangs (the pages'
   // setting, one SM per chain of a gang).  Symmetric shift also gets the
@@ -281,12 +313,14 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r) {
   if (!cyclic) cand.push_back(top);
   for (int m = (top / gang) * gang; m >= gang && (int)cand.size() < 16; m -= gang)
     if (cyclic || m != top) cand.push_back(m);
-  const HeadPlan hp = head_plan(mode, n, causal);
+  const HeadPlan hp = head_plan(mode, n, causal, split);
   const std::vector<int> hpred = head_pred(hp, n);
+  const std::vector<long long> order = split > 1 ? split_order(BH, (int)hp.off.size() - 1, split)
+                                                 : std::vector<long long>();
   int best = -1;
   long long best_ms = 0;
   for (int P : cand) {
-    SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic);
+    SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic, split > 1 ? &order : nullptr);
     if (sim.deadlock) continue;
     if (best < 0 || sim.makespan < best_ms || (sim.makespan == best_ms && P < best)) {
       best = P;

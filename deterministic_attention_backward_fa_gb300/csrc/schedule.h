@@ -33,13 +33,21 @@ long long num_tasks(int BH, int n, bool causal);
 
 // Builds chains for BH heads, simulates them on P CTAs with costs (c, r) and
 // fills `out`.  Returns an empty string on success, else the error.
+// split (shift and symmetric shift; 1 = none): each head's gang of chains
+// runs as `split` sub-gangs of consecutive chains.  A dQ tile's ranks go in
+// (sub-gang, step) order, and chains are dispatched sub-gang by sub-gang:
+// every head's sub-gang 0 first, then every head's sub-gang 1, and so on.  A
+// sub-gang keeps shift's property that no two of its chains reach one tile at
+// one step, and CTA counts that are multiples of the sub-gang become usable.
 std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
-                           Schedule *out);
+                           Schedule *out, int split = 1);
+// "" when `split` is valid for the schedule and n, else why not.
+std::string check_split(int mode, int n, int split);
 
 // Candidate CTA counts (P_max and multiples of the gang size up to it, capped
 // at the number of chains; only the multiples for shift), best simulated
 // makespan, ties to fewer CTAs.
-int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r);
+int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split = 1);
 
 // Fill (an extension beyond the pages' schedules) for shift (full mask) and
 // symmetric shift (causal): whole gangs of CTAs, as many as fit in P_max, run

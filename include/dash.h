@@ -159,6 +159,13 @@ typedef struct {
                             * semaphore alone measured faster); 2, 4, 8, 16 = that size
                             * (DASH_ERR_UNSUPPORTED if it does not divide the CTA count or the GPU cannot
                             * hold that many clusters at once).  Not with die_aware. */
+  int shift_split;         /* DASH_SCHED_SHIFT and DASH_SCHED_SYMMETRIC_SHIFT with the library's own table,
+                            * without fill: 0 or 1 = whole gangs (the pages' order); k > 1 = each head's gang
+                            * of chains runs as k sub-gangs of consecutive chains.  A dQ tile's ranks then go in
+                            * (sub-gang, step) order, every head's sub-gang 0 is dispatched before any sub-gang
+                            * 1, and the CTA count may be any multiple of the sub-gang.  Deterministic, with its
+                            * own bits.  k must divide the gang (n, or n/2 for symmetric shift);
+                            * DASH_ERR_UNSUPPORTED otherwise. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
@@ -285,6 +292,24 @@ dash_status_t dash_check_table(int BH, int n, int causal, int dq_chains, const i
 dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int cost_c,
                                     int cost_r, int32_t *tasks_out, int32_t *cta_off_out, int *ctas_out,
                                     int *shift_heads_out, int *fill_schedule_out, long long *makespan_out);
+
+/* Split gangs (dash_bwd_options_t.shift_split; an extension beyond the pages'
+ * schedules), host only: dash_build_schedule for shift or symmetric shift with
+ * each head's gang of chains run as `split` sub-gangs of consecutive slots.  A
+ * dQ tile's ranks go in (sub-gang, visiting step) order; chains are dispatched
+ * sub-gang by sub-gang (every head's sub-gang 0 first).  DASH_ERR_UNSUPPORTED
+ * for other schedules or a split that does not divide the gang (n, or n/2 for
+ * symmetric shift); DASH_ERR_SCHEDULE if the simulation deadlocks.  The table
+ * sizes are those of dash_build_schedule. */
+dash_status_t dash_build_split_schedule(int BH, int n, int causal, dash_schedule_t schedule, int split, int P,
+                                        int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
+                                        long long *makespan_out);
+
+/* The CTA count the backward uses with split gangs when num_ctas = 0: the
+ * multiple of the sub-gang up to max_ctas with the smallest simulated makespan
+ * (ties to fewer CTAs); -1 if the schedule or split is invalid.  Host only. */
+int dash_choose_split_ctas(int BH, int n, int causal, dash_schedule_t schedule, int split, int max_ctas,
+                           int cost_c, int cost_r);
 
 /* The CTA count the backward uses for a problem when num_ctas = 0: the
  * candidate (max_ctas, and the multiples of the schedule's gang size up to

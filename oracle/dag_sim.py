@@ -249,8 +249,48 @@ def schedule_tables(mode: str, BH: int, n: int, causal: bool, P: int, c: int = 4
     FLAG_FIRST marks the first task of a run on one KV tile, FLAG_LAST the
     last one.
     """
-    chains = all_chains(mode, BH, n, causal)
-    sim = simulate(chains, P, c, r, ordered=(mode != "atomic"))
+    return tables_of(all_chains(mode, BH, n, causal), P, c, r, ordered=(mode != "atomic"))
+
+
+def split_chains(mode: str, BH: int, n: int, causal: bool, split: int):
+    """Split gangs (an extension beyond the pages' schedules) of shift or
+    symmetric shift.  Each head's gang of chains (slot order) runs as ``split``
+    sub-gangs of consecutive slots.  The chains are dispatched sub-gang by
+    sub-gang: sub-gang 0 of every head, then sub-gang 1 of every head, and so
+    on.  A dQ tile's ranks go in (sub-gang, visiting step) order, so a
+    sub-gang adds to a tile only after the sub-gangs before it are done with
+    it; inside a sub-gang no two chains reach one tile at one step.  Returns
+    the chains in dispatch order, as ``all_chains`` does."""
+    if mode not in ("shift", "symmetric_shift"):
+        raise ScheduleError("split gangs apply to shift and symmetric shift only")
+    hc = head_chains(mode, n, causal)
+    if split < 1 or len(hc) % split:
+        raise ScheduleError("the split must divide the chains of a head's gang")
+    g = len(hc) // split
+    visits = {}
+    for slot, ch in enumerate(hc):
+        for step, (kv, q) in enumerate(ch):
+            visits.setdefault(q, []).append((slot // g, step, slot))
+    rank_of = {}
+    for q, lst in visits.items():
+        keys = [(sub, step) for sub, step, _ in lst]
+        if len(set(keys)) != len(keys):
+            raise ScheduleError(f"two chains of one sub-gang reach dQ tile {q} at the same step")
+        for rk, (sub, step, slot) in enumerate(sorted(lst)):
+            rank_of[(slot, step)] = rk
+    hr = [[rank_of[(slot, step)] for step in range(len(ch))] for slot, ch in enumerate(hc)]
+    return [(bh, hc[slot], hr[slot]) for sub in range(split) for bh in range(BH)
+            for slot in range(sub * g, (sub + 1) * g)]
+
+
+def split_tables(mode: str, BH: int, n: int, causal: bool, split: int, P: int, c: int = 4, r: int = 1):
+    """``schedule_tables`` for split gangs (``split_chains``)."""
+    return tables_of(split_chains(mode, BH, n, causal, split), P, c, r, ordered=True)
+
+
+def tables_of(chains, P: int, c: int, r: int, ordered: bool):
+    """Task tables of chains given in dispatch order (see ``schedule_tables``)."""
+    sim = simulate(chains, P, c, r, ordered=ordered)
     tasks = []
     cta_off = [0]
     for s in range(P):

@@ -272,3 +272,35 @@ def test_schedule_choice_rejects_bad_arguments():
     with pytest.raises(dash.DashError):
         dash.dash_choose_schedule(0, 4, False, 40)
     assert "dash_choose_schedule" in dash.dash_last_error()
+
+
+@pytest.mark.parametrize("mode,causal,BH,n", [("shift", False, 3, 8), ("shift", False, 2, 16), ("symmetric_shift", True, 3, 8),
+                                              ("symmetric_shift", True, 2, 16)])
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_split_generator_matches_simulator(mode, causal, BH, n, split):
+    gang = n if mode == "shift" else n // 2
+    for P in (gang // split, 2 * gang // split + 1, 40):
+        for c, r in ((4, 1), (2, 3)):
+            py_tasks, py_off, py_ms = d.split_tables(mode, BH, n, causal, split, P, c, r)
+            tasks, off, ms = dash.dash_build_split_schedule(BH, n, causal, mode, split, P, c, r)
+            assert np.array_equal(tasks, np.asarray(py_tasks, dtype=np.int32).reshape(-1, 4))
+            assert np.array_equal(off, np.asarray(py_off, dtype=np.int32)) and ms == py_ms
+
+
+def test_split_rejections_and_cta_choice():
+    with pytest.raises(dash.DashError) as ei:   # split gangs apply to the cyclic schedules only
+        dash.dash_build_split_schedule(2, 8, False, "serial", 2, 8)
+    assert ei.value.code == 2
+    with pytest.raises(dash.DashError) as ei:   # 3 does not divide a gang of 8
+        dash.dash_build_split_schedule(2, 8, False, "shift", 3, 8)
+    assert ei.value.code == 2
+    assert dash.dash_choose_split_ctas(2, 8, False, "shift", 3, 40) == -1
+    # the CTA count is a multiple of the sub-gang, chosen by simulated makespan
+    for split in (1, 2, 4):
+        P = dash.dash_choose_split_ctas(32, 32, False, "shift", split, 152, 8, 512)
+        assert P % (32 // split) == 0 and P <= 152
+        spans = {}
+        for cand in range(32 // split, 153, 32 // split):
+            spans[cand] = d.simulate(d.split_chains("shift", 32, 32, False, split), cand, 8, 512).makespan
+        best = min(spans.values())
+        assert spans[P] == best and P == min(c for c, s in spans.items() if s == best)

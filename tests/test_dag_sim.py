@@ -170,3 +170,62 @@ def test_fill_is_plain_shift_without_leftover_ctas():
     tasks, off, ms, hs, fm = d.fill_tables("shift", 8, 4, False, 16, 4, 1)   # 16 = 4 whole gangs
     assert (hs, fm) == (8, None)
     assert (tasks, off, ms) == d.schedule_tables("shift", 8, 4, False, 16, 4, 1)
+
+
+# ---- split gangs (an extension beyond the pages' schedules)
+
+@pytest.mark.parametrize("mode,causal,n", [("shift", False, 8), ("shift", False, 12), ("symmetric_shift", True, 8),
+                                           ("symmetric_shift", True, 16)])
+@pytest.mark.parametrize("split", [1, 2, 4])
+def test_split_gangs_cover_the_mask_and_order_tiles_by_subgang(mode, causal, n, split):
+    BH = 3
+    gang = n if mode == "shift" else n // 2
+    if gang % split:
+        with pytest.raises(d.ScheduleError):
+            d.split_chains(mode, BH, n, causal, split)
+        return
+    chains = d.split_chains(mode, BH, n, causal, split)
+    g = gang // split
+    # dispatch order: sub-gang 0 of every head, then sub-gang 1, ...
+    heads = [bh for bh, _, _ in chains]
+    assert heads == [bh for _ in range(split) for bh in range(BH) for _ in range(g)]
+    # the same tasks as the whole gangs: every (head, kv, q) of the mask once
+    plain = {(bh, kv, q) for bh, ch, _ in d.all_chains(mode, BH, n, causal) for kv, q in ch}
+    got = [(bh, kv, q) for bh, ch, _ in chains for kv, q in ch]
+    assert len(got) == len(set(got)) and set(got) == plain
+    # per tile the ranks are 0..k-1, and a sub-gang's ranks follow all of the one before it
+    by_tile = {}
+    for i, (bh, ch, rk) in enumerate(chains):
+        for (kv, q), rank in zip(ch, rk):
+            by_tile.setdefault((bh, q), []).append((rank, i // (BH * g)))
+    for tile, lst in by_tile.items():
+        ranks = sorted(r for r, _ in lst)
+        assert ranks == list(range(len(lst)))
+        subs_in_rank_order = [s for _, s in sorted(lst)]
+        assert subs_in_rank_order == sorted(subs_in_rank_order)
+    if split == 1:   # no split: exactly the pages' order
+        assert [rk for _, _, rk in chains] == [rk for _, _, rk in d.all_chains(mode, BH, n, causal)]
+
+
+@pytest.mark.parametrize("mode,causal,n,m", [("shift", False, 8, 3), ("shift", False, 16, 2),
+                                             ("symmetric_shift", True, 8, 3), ("symmetric_shift", True, 16, 2)])
+@pytest.mark.parametrize("split", [2, 4])
+@pytest.mark.parametrize("c,r", [(4, 1), (3, 2), (1, 1)])
+def test_split_gangs_never_wait_on_one_subgang_of_sms(mode, causal, n, m, split, c, r):
+    # with as many SMs as a sub-gang, sub-gangs run one after another in
+    # lockstep: no R waits, so the makespan is m * split sub-gangs of one
+    # chain length each, (c + r) per task (n tasks for shift, n + 1 for
+    # symmetric shift: the closed forms' T_full_opt and T_causal_opt per gang)
+    gang = n if mode == "shift" else n // 2
+    g = gang // split
+    sim = d.simulate(d.split_chains(mode, m, n, causal, split), g, c, r)
+    length = n if mode == "shift" else n + 1
+    assert sim.makespan == m * split * length * (c + r)
+    assert all(sim.r_start[t] == sim.c_end[t] for t in sim.c_end)
+
+
+def test_split_tables_of_one_equal_the_plain_tables():
+    for mode, causal, n, P in (("shift", False, 8, 16), ("symmetric_shift", True, 8, 12)):
+        a = d.split_tables(mode, 3, n, causal, 1, P, 4, 1)
+        b = d.schedule_tables(mode, 3, n, causal, P, 4, 1)
+        assert a == b
