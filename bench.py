@@ -13,9 +13,12 @@ are also timed with fill (shift_fill = 1: the SMs that whole gangs of their
 chains leave idle run some heads in the serial or descending order), under
 `extension_fill`, never in `value`; and with die-aware placement (die_aware = 1:
 each gang of chains on one die, its semaphores homed there) under
-`extension_die_aware`, never in `value`.  The long causal workload
+`extension_die_aware`, and with split gangs (shift_split = 4: each head's gang
+runs as four sub-gangs, so the CTA count need only be a multiple of a quarter
+gang) under `extension_split`, never in `value`.  The long causal workload
 (causal_s16384_d128) is timed in the same run, every schedule of its mask and
-symmetric shift with fill, and reported under `workloads` with its own ratio
+symmetric shift with fill, die-aware placement and split gangs, and reported
+under `workloads` with its own ratio
 to atomic and roofline fraction (`--also` names other workloads; '' skips it).
 
     python bench.py [--gpus N --steps K --warmup W] [--workload NAME] [--impl reference]
@@ -73,6 +76,8 @@ def parse():
                     help="skip timing shift and symmetric shift with fill (shift_fill = 1)")
     ap.add_argument("--no-die-aware", action="store_true",
                     help="skip timing shift and symmetric shift with die-aware placement (die_aware = 1)")
+    ap.add_argument("--split", type=int, default=4,
+                    help="split gangs timed for shift and symmetric shift (shift_split; 0 or 1 skips)")
     ap.add_argument("--also", default="causal_s16384_d128",
                     help="comma-separated further workloads timed in the same run and reported under "
                          "`workloads` (every schedule of the mask and fill; '' for none)")
@@ -228,9 +233,19 @@ def run_reference(args, rank, world):
     return 0
 
 
-def best_with_extensions(results, two_chains, fill, best, world, peak, die=None):
+def split_of(w, sched, k):
+    """k if split gangs of k apply to the schedule on this workload (k divides its gang), else 0."""
+    if k <= 1 or sched not in ("shift", "symmetric_shift") or sched not in w.schedules:
+        return 0
+    n = w.S // w.tile
+    gang = n // 2 if sched == "symmetric_shift" else n
+    return k if gang % k == 0 else 0
+
+
+def best_with_extensions(results, two_chains, fill, best, world, peak, die=None, split=None):
     """The fastest deterministic layout including the extensions (never in `value`)."""
     cands = {best: results[best]}
+    cands.update({f"{s}+split": r for s, r in (split or {}).items()})
     cands.update({f"{s}+fill": r for s, r in fill.items()})
     cands.update({f"{s}+two_dq_chains": r for s, r in two_chains.items()})
     cands.update({f"{s}+die_aware": r for s, r in (die or {}).items()})
@@ -259,31 +274,32 @@ def run_sweep(args, dash):
     peaks, _ = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     for w in workloads.pages_sweep():
-        q, k, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
-        o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
+        q, k_, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
+        o, lse = dash.attn_fwd(q, k_, v, w.causal, w.scale)
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-        res, fill = {}, {}
-        runs = [(s, 0) for s in w.schedules]
-        runs += [(s, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+        res, fill, split = {}, {}, {}
+        runs = [(s, 0, 0) for s in w.schedules]
+        runs += [(s, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+        runs += [(s, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift") if split_of(w, s, args.split)]
         with ClockSampler(0) as clk:
-            for sched, shift_fill in runs:
+            for sched, shift_fill, k in runs:
                 for _ in range(args.warmup):
                     flush.fill_(1)
-                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                          shift_fill=shift_fill)
+                    dash.dash_attn_bwd_ex(q, k_, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                          shift_fill=shift_fill, shift_split=k)
                 dash.dash_sync_status()
                 ms = []
                 for _ in range(args.steps):
                     flush.fill_(1)
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
-                    dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                          shift_fill=shift_fill)
+                    dash.dash_attn_bwd_ex(q, k_, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
+                                          shift_fill=shift_fill, shift_split=k)
                     b.record(stream)
                     b.synchronize()
                     ms.append(a.elapsed_time(b))
                 dash.dash_sync_status()
-                (fill if shift_fill else res)[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
+                (split if k else fill if shift_fill else res)[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
         det = {s: t for s, t in res.items() if s != "atomic"}
         best = max(det, key=det.get)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -293,19 +309,21 @@ def run_sweep(args, dash):
                           "statistic": f"median of {args.steps} steps", "schedules": res,
                           "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
                           "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
+                          "extension_split": {s: {"tflops": t, "split": args.split, "vs_atomic": t / res["atomic"]}
+                                              for s, t in split.items()} or None,
                           "runtime_choice": choice, "clocks": clk.summary()}), flush=True)
-        del q, k, v, do, o, lse, dq, dk, dv
+        del q, k_, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
 
 
 def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
-    """Times each (schedule, dq_chains, shift_fill) of `runs`: W warm-up steps, then K steps, each
+    """Times each (schedule, dq_chains, shift_fill, die_aware, shift_split) of `runs`: W warm-up steps, then K steps, each
     bracketed by CUDA events on the launching stream, with the main kernel's own events inside."""
     q, k, v, o, do, lse, dq, dk, dv = tensors
     flops = w.flops()
-    results, two_chains, fill, die = {}, {}, {}, {}
+    results, two_chains, fill, die, split = {}, {}, {}, {}, {}
     launches = 0
-    for sched, chains, shift_fill, die_aware in runs:
+    for sched, chains, shift_fill, die_aware, ks in runs:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -315,7 +333,7 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         for _ in range(args.warmup):
             flush.fill_(1)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                  dq_chains=chains, shift_fill=shift_fill, die_aware=die_aware)
+                                  dq_chains=chains, shift_fill=shift_fill, die_aware=die_aware, shift_split=ks)
         dash.dash_sync_status()
         barrier()
         torch.cuda.synchronize()
@@ -324,7 +342,7 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
             evs[i][0].record(stream)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
                                   main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
-                                  shift_fill=shift_fill, die_aware=die_aware)
+                                  shift_fill=shift_fill, die_aware=die_aware, shift_split=ks)
             evs[i][3].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -333,10 +351,12 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
         main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
         total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-        (die if die_aware else fill if shift_fill else results if chains == 1 else two_chains)[sched] = {
-            "ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
-            "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
-    return results, two_chains, fill, die, launches
+        out = split if ks else die if die_aware else fill if shift_fill else results if chains == 1 else two_chains
+        out[sched] = {"ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
+                      "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
+        if ks:
+            out[sched]["split"] = ks
+    return results, two_chains, fill, die, split, launches
 
 
 def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
@@ -347,15 +367,16 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
     o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
     dash.dash_sync_status()
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    runs = [(s, 1, 0, 0) for s in w.schedules]
-    runs += [(s, 1, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
-    runs += [(s, 1, 0, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_die_aware]
-    results, _, fill, die, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
+    runs = [(s, 1, 0, 0, 0) for s in w.schedules]
+    runs += [(s, 1, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_die_aware]
+    runs += [(s, 1, 0, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift") if split_of(w, s, args.split)]
+    results, _, fill, die, split, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
                                                 stream, world, dev, barrier)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     atomic = results["atomic"]
-    for r in list(results.values()) + list(fill.values()) + list(die.values()):
+    for r in list(results.values()) + list(fill.values()) + list(die.values()) + list(split.values()):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"]
     det = {s: r for s, r in results.items() if s != "atomic"}
     best = max(det, key=lambda s: det[s]["tflops"])
@@ -367,6 +388,8 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
            "ratio_vs_atomic": results[best]["vs_atomic"], "schedules": results,
            "extension_fill": fill or None,
            "extension_die_aware": die or None,
+           "extension_split": split or None,
+           "best_with_extensions": best_with_extensions(results, {}, fill, best, world, peak, die, split),
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                         "frac": achieved / peak, "kernel": "dash_bwd_main",
                         "peak_source": f"{peak_kind} bf16_tflops (burst)"},
@@ -429,12 +452,14 @@ def main():
             pass
 
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
-    runs = [(s, 1, 0, 0) for s in scheds]
-    runs += [(s, 2, 0, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
-    runs += [(s, 1, 1, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
-    runs += [(s, 1, 0, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_die_aware]
+    runs = [(s, 1, 0, 0, 0) for s in scheds]
+    runs += [(s, 2, 0, 0, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
+    runs += [(s, 1, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_die_aware]
+    runs += [(s, 1, 0, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift")
+             if s in scheds and split_of(w, s, args.split)]
     with ClockSampler(gpu_index) as clk:
-        results, two_chains, fill, die, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
+        results, two_chains, fill, die, split, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
                                                              args, flush, stream, world, dev, barrier)
         also = {}
         for name in [x for x in args.also.split(",") if x and x != w.name]:
@@ -446,7 +471,8 @@ def main():
     det = {s: r for s, r in results.items() if s != "atomic"} or results
     best = max(det, key=lambda s: det[s]["tflops"])
     atomic = results.get("atomic")
-    for s, r in list(results.items()) + list(two_chains.items()) + list(fill.items()) + list(die.items()):
+    for s, r in (list(results.items()) + list(two_chains.items()) + list(fill.items()) + list(die.items())
+                 + list(split.items())):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
     choice = None
     if atomic and "serial" in results:
@@ -495,7 +521,7 @@ def main():
                        "flops_per_step": flops},
             "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
             "ratio_vs_atomic": results[best]["vs_atomic"],
-            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak, die),
+            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak, die, split),
             "schedules": results,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
@@ -507,6 +533,7 @@ def main():
             "extension_two_dq_chains": two_chains or None,
             "extension_die_aware": die or None,
             "extension_fill": fill or None,
+            "extension_split": split or None,
             "runtime_choice": choice,
             "gpu_launches": launches,
             "clocks": clocks,

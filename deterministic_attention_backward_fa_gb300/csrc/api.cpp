@@ -340,8 +340,9 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   }
   if (opt && (opt->die_aware < 0 || opt->die_aware > 1)) return fail(DASH_ERR_INVALID_ARG, "die_aware must be 0 or 1");
   const bool die_aware = opt && opt->die_aware == 1;
-  if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks))
-    return fail(DASH_ERR_UNSUPPORTED, "die_aware applies to shift and symmetric shift, without fill or a supplied table");
+  if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks || split > 1))
+    return fail(DASH_ERR_UNSUPPORTED,
+                "die_aware applies to shift and symmetric shift, without fill, split gangs or a supplied table");
   const int want_cluster = opt ? opt->cluster_size : 0;
   if (want_cluster < 0 || want_cluster > 16 || (want_cluster & (want_cluster - 1)))
     return fail(DASH_ERR_INVALID_ARG, "cluster_size must be 0 (auto), 1, 2, 4, 8 or 16");

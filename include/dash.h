@@ -165,7 +165,7 @@ typedef struct {
                             * (sub-gang, step) order, every head's sub-gang 0 is dispatched before any sub-gang
                             * 1, and the CTA count may be any multiple of the sub-gang.  Deterministic, with its
                             * own bits.  k must divide the gang (n, or n/2 for symmetric shift);
-                            * DASH_ERR_UNSUPPORTED otherwise. */
+                            * DASH_ERR_UNSUPPORTED otherwise, and with die_aware. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.

@@ -111,6 +111,17 @@ def test_error_codes_without_gpu():
     opt = dash.BwdOptions(0, 0, 0, 0, 0, None, None, None, None, None, 3)
     assert L.dash_attn_bwd_ex(*([fake] * 9), 1, 1, 128, 64, 0, 0.1, 1, ctypes.byref(opt), nul) == 1
     assert "dq_chains" in dash.dash_last_error()
+    # split gangs: a k that does not divide the gang, a negative k, and k with fill or die-aware placement
+    # (S = 1024, tile 128: a shift gang of 8 chains) are rejected before any CUDA call
+    for fields, code, words in [({"shift_split": 3}, 2, "divide"), ({"shift_split": -1}, 1, "shift_split"),
+                                ({"shift_split": 2, "shift_fill": 1}, 2, "without fill"),
+                                ({"shift_split": 2, "die_aware": 1}, 2, "split gangs")]:
+        opt = dash.BwdOptions()
+        for f, x in fields.items():
+            setattr(opt, f, x)
+        opt.tile = 128
+        assert L.dash_attn_bwd_ex(*([fake] * 9), 1, 1, 1024, 64, 0, 0.1, 3, ctypes.byref(opt), nul) == code
+        assert words in dash.dash_last_error()
     # more tasks than the 32-bit task tables index: 2^16 heads at S = 2^20 (full mask, n = 8192)
     assert L.dash_attn_bwd(*([fake] * 9), 1, 1 << 16, 1 << 20, 64, 0, 0.1, 1, nul) == 2
     assert "32-bit" in dash.dash_last_error()

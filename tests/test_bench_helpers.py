@@ -22,6 +22,20 @@ def test_best_with_extensions_picks_the_fastest_layout():
     assert b["schedule"] == "shift+two_dq_chains"
     b = bench.best_with_extensions(res, {}, {}, "shift", 2, 2000.0)   # whole-job value over two GPUs
     assert b["schedule"] == "shift" and abs(b["pct_bf16_peak"] - 18.75) < 1e-9
+    split = {"shift": {"tflops": 870.0, "vs_atomic": 0.967, "split": 4}}
+    b = bench.best_with_extensions(res, two, fill, "shift", 1, 2000.0, split=split)
+    assert b["schedule"] == "shift+split" and b["tflops"] == 870.0
+
+
+def test_split_of_needs_a_divisor_of_the_gang():
+    full, causal = workloads.WORKLOADS["full_s4096_d128"], workloads.WORKLOADS["causal_s8192_d64"]
+    assert bench.split_of(full, "shift", 4) == 4             # a gang of 32 chains
+    assert bench.split_of(full, "shift", 3) == 0
+    assert bench.split_of(full, "shift", 1) == 0             # 1 = whole gangs, not timed as an extension
+    assert bench.split_of(full, "serial", 4) == 0
+    assert bench.split_of(full, "symmetric_shift", 4) == 0   # not a schedule of the full mask
+    n = causal.S // causal.tile
+    assert bench.split_of(causal, "symmetric_shift", 4) == (4 if (n // 2) % 4 == 0 else 0)
 
 
 def test_runtime_choice_uses_the_fitted_costs():

@@ -148,6 +148,61 @@ def test_fill_heads_equal_their_own_schedules(wname, sched, chains):
         assert_close(f"{sched} with fill {name}[{b_},{h_}] rows", x[BH - 1][rows], r)
 
 
+# split gangs (an extension): S, D, tile, mask, schedule, split; several
+# sub-gangs per head, ragged tails, both head dims
+SPLIT = [(512, 64, 64, False, "shift", 2), (500, 64, 64, False, "shift", 4),
+         (1000, 64, 64, True, "symmetric_shift", 4), (1024, 128, 128, True, "symmetric_shift", 2),
+         (700, 128, 128, False, "shift", 2)]
+
+
+@pytest.mark.parametrize("S,D,tile,causal,sched,split", SPLIT,
+                         ids=[f"{s}_s{S}_d{D}_k{k}" for S, D, _, _, s, k in SPLIT])
+def test_split_gangs_match_oracle(S, D, tile, causal, sched, split):
+    # every output against the oracle, with one and two dQ chains; the bits do
+    # not depend on the CTA count (the library's choice, one sub-gang, three)
+    H = 3
+    n = (S + tile - 1) // tile
+    g = (n // 2 if sched == "symmetric_shift" else n) // split
+    P = Problem(1, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    q, k, v, do = P.f64
+    ref = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    for chains in (1, 2):
+        first = None
+        for ctas in (0, g, 3 * g):
+            got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, dq_accum=True,
+                                dq_chains=chains, shift_split=split, num_ctas=ctas)
+            dash.dash_sync_status()
+            if first is None:
+                first = got
+                for name, x, r in zip(("dQ", "dK", "dV"), got[:3], ref):
+                    assert_close(f"{sched} split {split}, {chains} chain(s) {name}", x, r)
+            else:
+                assert all(torch.equal(a, b) for a, b in zip(first, got)), f"{ctas} CTAs changed the bits"
+
+
+@pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
+def test_split_gangs_full_size(wname, sched):
+    # split gangs of four at full size, on the CTA count the library picks:
+    # sampled rows of the first and last heads against the row-wise oracle,
+    # and the same bits on a second run
+    w = workloads.WORKLOADS[wname]
+    BH = w.B * w.H
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    run = lambda: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile, shift_split=4)
+    got, again = run(), run()
+    dash.dash_sync_status()
+    assert all(torch.equal(a, b) for a, b in zip(got, again))
+    q, k, v, do = P.f64
+    rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1})
+    for b_, h_ in ((0, 0), (w.B - 1, w.H - 1)):
+        oh, lh = o[b_, h_].double().cpu().numpy(), lse[b_, h_].double().cpu().numpy()
+        ref = A.backward_rows(q[b_, h_], k[b_, h_], v[b_, h_], oh, do[b_, h_], lh, w.causal, P.scale, rows)
+        for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert_close(f"{sched} split 4 {name}[{b_},{h_}] rows", x[b_, h_][rows], r)
+
+
 def _red_add_f32(acc, x):
     """fp32 add as red.global.add.f32 performs it: round to nearest even, with
     subnormal inputs and results flushed to (signed) zero."""
@@ -184,12 +239,18 @@ def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
                                 tasks=one, cta_off=np.array([0, 1], dtype=np.int32))[3]
             dash.dash_sync_status()
             part[(bh, kv, q)] = acc.reshape(BH, S, D)[bh, q * tile:(q + 1) * tile].cpu().numpy()
-    for sched in ("serial", "descending_q", "symmetric_shift" if causal else "shift"):
-        chains_ = d.head_chains(sched, n, causal)
-        rank = {t: rk for ch, rks in zip(chains_, d.head_ranks(sched, n, causal, chains_)) for t, rk in zip(ch, rks)}
+    cyclic = "symmetric_shift" if causal else "shift"
+    # the pages' orders, and split gangs of two (an extension) for the cyclic schedule
+    for sched, split in (("serial", 1), ("descending_q", 1), (cyclic, 1), (cyclic, 2)):
+        if split == 1:
+            chains_ = d.head_chains(sched, n, causal)
+            ranked = zip(chains_, d.head_ranks(sched, n, causal, chains_))
+        else:
+            ranked = [(ch, rks) for _, ch, rks in d.split_chains(sched, 1, n, causal, split)]
+        rank = {t: rk for ch, rks in ranked for t, rk in zip(ch, rks)}
         for nch in (1, 2):
             got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, dq_accum=True,
-                                dq_chains=nch)[3]
+                                dq_chains=nch, shift_split=split)[3]
             dash.dash_sync_status()
             got = got.reshape(BH, S, D).cpu().numpy()
             for bh in range(BH):
@@ -202,7 +263,8 @@ def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
                         sums[c] = x.copy() if sums[c] is None else _red_add_f32(sums[c], x)
                     want = sums[0] if nch == 1 or sums[1] is None else (sums[0] + sums[1]).astype(np.float32)
                     assert np.array_equal(got[bh, q * tile:(q + 1) * tile], want), \
-                        f"{sched}, {nch} chain(s): head {bh}, dQ tile {q} differs from the rank-order sum"
+                        f"{sched} (split {split}), {nch} chain(s): head {bh}, dQ tile {q} differs from the " \
+                        "rank-order sum"
 
 
 LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
