@@ -13,9 +13,10 @@ are also timed with fill (shift_fill = 1: the SMs that whole gangs of their
 chains leave idle run some heads in the serial or descending order), under
 `extension_fill`, never in `value`; and with die-aware placement (die_aware = 1:
 each gang of chains on one die, its semaphores homed there) under
-`extension_die_aware`, and with split gangs (shift_split = 4: each head's gang
-runs as four sub-gangs, so the CTA count need only be a multiple of a quarter
-gang) under `extension_split`, never in `value`.  The long causal workload
+`extension_die_aware`, and with split gangs (shift_split = -1: each head's gang
+runs as k sub-gangs, k picked by the library's simulation, so that the CTA
+count need only be a multiple of a sub-gang) under `extension_split`, never in
+`value`.  The long causal workload
 (causal_s16384_d128) is timed in the same run, every schedule of its mask and
 symmetric shift with fill, die-aware placement and split gangs, and reported
 under `workloads` with its own ratio
@@ -76,8 +77,9 @@ def parse():
                     help="skip timing shift and symmetric shift with fill (shift_fill = 1)")
     ap.add_argument("--no-die-aware", action="store_true",
                     help="skip timing shift and symmetric shift with die-aware placement (die_aware = 1)")
-    ap.add_argument("--split", type=int, default=4,
-                    help="split gangs timed for shift and symmetric shift (shift_split; 0 or 1 skips)")
+    ap.add_argument("--split", type=int, default=-1,
+                    help="split gangs timed for shift and symmetric shift (shift_split: -1 = the library's "
+                         "choice, k > 1 = k sub-gangs, 0 or 1 skips)")
     ap.add_argument("--also", default="causal_s16384_d128",
                     help="comma-separated further workloads timed in the same run and reported under "
                          "`workloads` (every schedule of the mask and fill; '' for none)")
@@ -234,12 +236,20 @@ def run_reference(args, rank, world):
 
 
 def split_of(w, sched, k):
-    """k if split gangs of k apply to the schedule on this workload (k divides its gang), else 0."""
-    if k <= 1 or sched not in ("shift", "symmetric_shift") or sched not in w.schedules:
+    """The shift_split to time for the schedule on this workload: -1 (the library's choice) or k where k
+    divides its gang; 0 where split gangs do not apply."""
+    if k in (0, 1) or sched not in ("shift", "symmetric_shift") or sched not in w.schedules:
         return 0
+    if k == -1:
+        return -1
     n = w.S // w.tile
     gang = n // 2 if sched == "symmetric_shift" else n
-    return k if gang % k == 0 else 0
+    return k if k > 1 and gang % k == 0 else 0
+
+
+def split_chosen(dash, w, sched, k, sms):
+    """The split a run with shift_split = k uses (-1 resolved through the library's choice)."""
+    return dash.dash_choose_split(w.B * w.H, w.S // w.tile, w.causal, sched, sms)[0] if k == -1 else k
 
 
 def best_with_extensions(results, two_chains, fill, best, world, peak, die=None, split=None):
@@ -309,7 +319,8 @@ def run_sweep(args, dash):
                           "statistic": f"median of {args.steps} steps", "schedules": res,
                           "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
                           "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
-                          "extension_split": {s: {"tflops": t, "split": args.split, "vs_atomic": t / res["atomic"]}
+                          "extension_split": {s: {"tflops": t, "vs_atomic": t / res["atomic"],
+                                                  "split": split_chosen(dash, w, s, args.split, sms)}
                                               for s, t in split.items()} or None,
                           "runtime_choice": choice, "clocks": clk.summary()}), flush=True)
         del q, k_, v, do, o, lse, dq, dk, dv
@@ -355,7 +366,8 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         out[sched] = {"ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
                       "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
         if ks:
-            out[sched]["split"] = ks
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            out[sched]["split"] = split_chosen(dash, w, sched, ks, sms)
     return results, two_chains, fill, die, split, launches
 
 

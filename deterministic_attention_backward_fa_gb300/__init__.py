@@ -71,6 +71,7 @@ _SIGS = {
     "dash_choose_ctas": ([_I] * 7, _I),
     "dash_build_split_schedule": ([_I] * 8 + [_P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_split_ctas": ([_I] * 8, _I),
+    "dash_choose_split": ([_I] * 8 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_check_table": ([_I] * 4 + [_P, _P, _I], _I),
     "dash_fit_costs": ([_I] * 4 + [ctypes.c_double] * 2 + [ctypes.POINTER(_I)] * 2, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
@@ -175,7 +176,8 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     main kernel fills with per-task phase stamps.  ``die_aware=1`` places each gang of a shift schedule
     on one die with its semaphores homed there; ``cluster_size`` (0 or 1 = none; 2, 4, 8, 16) sets the thread-block
     clusters whose ranks hand the dQ turn over through shared memory; ``shift_split=k`` runs each gang of a
-    shift or symmetric-shift schedule as k sub-gangs (see dash_bwd_options_t)."""
+    shift or symmetric-shift schedule as k sub-gangs, and ``shift_split=-1`` lets the library pick k by
+    simulated makespan (see dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
@@ -291,6 +293,16 @@ def dash_build_split_schedule(BH: int, n: int, causal: bool, schedule, split: in
     _check(lib().dash_build_split_schedule(BH, n, int(causal), _sched(schedule), split, P, cost_c, cost_r,
                                            tasks.ctypes.data, off.ctypes.data, ctypes.byref(ms)))
     return tasks[:nt], off, ms.value
+
+
+def dash_choose_split(BH: int, n: int, causal: bool, schedule, max_ctas: int, num_ctas: int = 0, cost_c: int = 4,
+                      cost_r: int = 1):
+    """Host-only.  The split that ``shift_split=-1`` picks: returns (k, CTA count, simulated makespan), k = -1
+    where split gangs do not apply."""
+    P, ms = _I(0), ctypes.c_longlong(0)
+    k = lib().dash_choose_split(BH, n, int(causal), _sched(schedule), max_ctas, num_ctas, cost_c, cost_r,
+                                ctypes.byref(P), ctypes.byref(ms))
+    return int(k), P.value, ms.value
 
 
 def dash_choose_split_ctas(BH: int, n: int, causal: bool, schedule, split: int, max_ctas: int, cost_c: int = 4,

@@ -331,8 +331,13 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   if (opt && (opt->shift_fill < 0 || opt->shift_fill > 1))
     return fail(DASH_ERR_INVALID_ARG, "shift_fill must be 0 or 1");
   const bool fill = (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT) && opt && opt->shift_fill == 1;
+  if (opt && opt->shift_split < -1) return fail(DASH_ERR_INVALID_ARG, "shift_split must be >= -1");
+  // -1: the split is chosen by simulation, where split gangs apply (shift and
+  // symmetric shift on the library's own table, without fill or die-aware
+  // placement); elsewhere it means whole gangs
+  const bool split_auto = opt && opt->shift_split == -1 && !fill && !opt->tasks && opt->die_aware != 1 &&
+                          (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT);
   const int split = (opt && opt->shift_split > 1) ? opt->shift_split : 1;
-  if (opt && opt->shift_split < 0) return fail(DASH_ERR_INVALID_ARG, "shift_split must be >= 0");
   if (split > 1) {
     if (fill || (opt && opt->tasks)) return fail(DASH_ERR_UNSUPPORTED, "shift_split applies to the library's own table, without fill");
     why = dash::check_split(mode, n, split);
@@ -386,7 +391,8 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
   } else {
     const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
     if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
-    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains, fill ? -1 : split);
+    auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains,
+                               fill ? -1 : split_auto ? -2 : split);
     auto &ent = g_sched[key];
     if (!ent) {
       std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
@@ -396,6 +402,16 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       // With fill, the SMs that whole gangs leave idle run other heads in the
       // serial order (num_ctas, if given, is the CTA budget).
       int Puse = want;
+      int use_split = split;
+      if (split_auto) {
+        int Pk = 0;
+        use_split = dash::choose_split(BH, n, causal != 0, mode, sms, c, r, want, &Pk, nullptr);
+        if (use_split < 1) {
+          g_sched.erase(key);
+          return fail(DASH_ERR_UNSUPPORTED, "no split of the gang runs this schedule on up to %d CTAs", sms);
+        }
+        Puse = Pk;
+      }
       if (!Puse && !fill && chains == 2 && mode == DASH_SCHED_SHIFT)
         Puse = (int)std::min<long long>(sms, (long long)BH * n);
       if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r, split);
@@ -408,7 +424,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
         why = dash::build_fill(BH, n, causal != 0, mode, want ? want : sms, c, r, &sch, nullptr, nullptr);
         Puse = sch.P;
       } else {
-        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch, split);
+        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch, use_split);
       }
       if (!why.empty()) {
         g_sched.erase(key);
@@ -810,6 +826,13 @@ dash_status_t dash_build_split_schedule(int BH, int n, int causal, dash_schedule
   std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
   if (makespan_out) *makespan_out = s.makespan;
   return DASH_OK;
+}
+
+int dash_choose_split(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int num_ctas, int cost_c,
+                      int cost_r, int *ctas_out, long long *makespan_out) {
+  if (cost_c < 1 || cost_r < 1 || num_ctas < 0 || num_ctas > max_ctas) return -1;
+  return dash::choose_split(BH, n, causal != 0, (int)schedule, max_ctas, cost_c, cost_r, num_ctas, ctas_out,
+                            makespan_out);
 }
 
 int dash_choose_split_ctas(int BH, int n, int causal, dash_schedule_t schedule, int split, int max_ctas, int cost_c,

@@ -297,7 +297,13 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
   return "";
 }
 
-int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split) {
+namespace {
+
+// choose_ctas with the winner's simulated makespan in *ms, among at most
+// max_cand candidates; with fixed_P > 0 that CTA count is the only candidate
+// (for shift, only if it is a multiple of the gang).
+int best_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split, int fixed_P, int max_cand,
+              long long *ms) {
   if (split < 1) split = 1;
   if (!check_mode(mode, n, causal).empty() || !check_split(mode, n, split).empty() || BH < 1 || P_max < 1) return -1;
   const long long nch = (long long)BH * chains_per_head(mode, n);
@@ -310,9 +316,14 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, i
   const bool cyclic = (mode == kShift);
   std::vector<int> cand;
   const int top = (int)std::min<long long>(P_max, nch);
-  if (!cyclic) cand.push_back(top);
-  for (int m = (top / gang) * gang; m >= gang && (int)cand.size() < 16; m -= gang)
-    if (cyclic || m != top) cand.push_back(m);
+  if (fixed_P > 0) {
+    if (cyclic && fixed_P % gang) return -1;
+    cand.push_back(fixed_P);
+  } else {
+    if (!cyclic) cand.push_back(top);
+    for (int m = (top / gang) * gang; m >= gang && (int)cand.size() < max_cand; m -= gang)
+      if (cyclic || m != top) cand.push_back(m);
+  }
   const HeadPlan hp = head_plan(mode, n, causal, split);
   const std::vector<int> hpred = head_pred(hp, n);
   const std::vector<long long> order = split > 1 ? split_order(BH, (int)hp.off.size() - 1, split)
@@ -327,7 +338,47 @@ int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, i
       best_ms = sim.makespan;
     }
   }
+  if (ms) *ms = best_ms;
   return best;
+}
+
+}  // namespace
+
+int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split) {
+  return best_ctas(BH, n, causal, mode, P_max, c, r, split, 0, 16, nullptr);
+}
+
+int choose_split(int BH, int n, bool causal, int mode, int P_max, int c, int r, int fixed_P, int *P_out,
+                 long long *makespan_out) {
+  if (mode != kShift && mode != kSymmetricShift) return -1;
+  if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1 || c < 1 || r < 1) return -1;
+  const int gang = chains_per_head(mode, n);
+  int best_k = -1, best_P = 0;
+  bool best_whole = false;
+  long long best_ms = 0;
+  for (int k = 1; k <= gang; ++k) {
+    if (gang % k) continue;
+    long long ms = 0;
+    // the four largest candidate counts of each k: a split gang's closed form
+    // has no waits, so fewer CTAs only lose SMs
+    const int P = best_ctas(BH, n, causal, mode, P_max, c, r, k, fixed_P, 4, &ms);
+    if (P < 1) continue;
+    // On a tie, sub-gangs that fill the CTAs side by side win: a sub-gang
+    // spread over time waits on its neighbours' hops, which the task costs
+    // do not price.
+    const bool whole = P % (gang / k) == 0;
+    if (best_k < 0 || ms < best_ms || (ms == best_ms && whole && !best_whole)) {
+      best_k = k;
+      best_P = P;
+      best_ms = ms;
+      best_whole = whole;
+    }
+  }
+  if (best_k > 0) {
+    if (P_out) *P_out = best_P;
+    if (makespan_out) *makespan_out = best_ms;
+  }
+  return best_k;
 }
 
 std::string build_fill(int BH, int n, bool causal, int mode, int P_max, int c, int r, Schedule *out,

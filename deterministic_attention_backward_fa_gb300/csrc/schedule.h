@@ -49,6 +49,17 @@ std::string check_split(int mode, int n, int split);
 // makespan, ties to fewer CTAs.
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split = 1);
 
+// Split gangs chosen by simulation (shift and symmetric shift): every split k
+// that divides the gang, each on the best of choose_ctas' four largest
+// candidate CTA counts (or on fixed_P CTAs when fixed_P > 0; for shift only
+// where fixed_P is a multiple of the sub-gang), and the k of the smallest
+// simulated makespan; ties go first to a k whose sub-gang divides its CTA
+// count, then to the smaller k (so 1, whole gangs, wins a plain tie).
+// Fills the CTA count and the makespan; returns k, or -1 on invalid arguments
+// or when no k runs.
+int choose_split(int BH, int n, bool causal, int mode, int P_max, int c, int r, int fixed_P, int *P_out,
+                 long long *makespan_out);
+
 // Fill (an extension beyond the pages' schedules) for shift (full mask) and
 // symmetric shift (causal): whole gangs of CTAs, as many as fit in P_max, run
 // `mode` for the first `shift_heads` heads; the CTAs that whole gangs leave

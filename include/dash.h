@@ -165,7 +165,9 @@ typedef struct {
                             * (sub-gang, step) order, every head's sub-gang 0 is dispatched before any sub-gang
                             * 1, and the CTA count may be any multiple of the sub-gang.  Deterministic, with its
                             * own bits.  k must divide the gang (n, or n/2 for symmetric shift);
-                            * DASH_ERR_UNSUPPORTED otherwise, and with die_aware. */
+                            * DASH_ERR_UNSUPPORTED otherwise, and with die_aware.  -1 = the library picks k
+                            * by simulated makespan (dash_choose_split), where split gangs apply; with
+                            * another schedule, fill, die_aware or a supplied table it means 0. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
@@ -310,6 +312,18 @@ dash_status_t dash_build_split_schedule(int BH, int n, int causal, dash_schedule
  * (ties to fewer CTAs); -1 if the schedule or split is invalid.  Host only. */
 int dash_choose_split_ctas(int BH, int n, int causal, dash_schedule_t schedule, int split, int max_ctas,
                            int cost_c, int cost_r);
+
+/* The split that shift_split = -1 picks (an extension): for shift and
+ * symmetric shift, every k that divides the gang (n, or n/2 for symmetric
+ * shift), each on its dash_choose_split_ctas CTA count (on num_ctas CTAs when
+ * num_ctas > 0), and the k whose simulated makespan is smallest; ties go
+ * first to a k whose sub-gang divides its CTA count (sub-gangs side by side,
+ * none spread over time), then to the smaller k (1 = whole gangs).  Writes
+ * the CTA count and makespan; returns k,
+ * or -1 for another schedule, invalid arguments, or num_ctas > max_ctas.
+ * Host only. */
+int dash_choose_split(int BH, int n, int causal, dash_schedule_t schedule, int max_ctas, int num_ctas, int cost_c,
+                      int cost_r, int *ctas_out, long long *makespan_out);
 
 /* The CTA count the backward uses for a problem when num_ctas = 0: the
  * candidate (max_ctas, and the multiples of the schedule's gang size up to

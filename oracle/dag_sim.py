@@ -41,6 +41,10 @@ conflict-free schedules never wait at P = n, and coverage of every tile.
 fill_tables (an extension) is pinned by coverage, by each head's ranks
 equalling its own schedule's, and by brute force over every split of the
 heads; fit_costs by recovering the r that produced simulated makespans.
+split_chains (an extension) is pinned by coverage, by each tile's ranks
+running sub-gang after sub-gang, by equality with the plain chains for a split
+of one, and by the closed form m * split * len * (c + r) with no wait on as
+many SMs as a sub-gang (the overview's optimal forms, section 3, per gang).
 """
 from __future__ import annotations
 

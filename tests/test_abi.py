@@ -113,7 +113,7 @@ def test_error_codes_without_gpu():
     assert "dq_chains" in dash.dash_last_error()
     # split gangs: a k that does not divide the gang, a negative k, and k with fill or die-aware placement
     # (S = 1024, tile 128: a shift gang of 8 chains) are rejected before any CUDA call
-    for fields, code, words in [({"shift_split": 3}, 2, "divide"), ({"shift_split": -1}, 1, "shift_split"),
+    for fields, code, words in [({"shift_split": 3}, 2, "divide"), ({"shift_split": -2}, 1, "shift_split"),
                                 ({"shift_split": 2, "shift_fill": 1}, 2, "without fill"),
                                 ({"shift_split": 2, "die_aware": 1}, 2, "split gangs")]:
         opt = dash.BwdOptions()
@@ -315,3 +315,43 @@ def test_split_rejections_and_cta_choice():
             spans[cand] = d.simulate(d.split_chains("shift", 32, 32, False, split), cand, 8, 512).makespan
         best = min(spans.values())
         assert spans[P] == best and P == min(c for c, s in spans.items() if s == best)
+
+
+@pytest.mark.parametrize("BH,n,causal,mode,P_max", [(4, 8, False, "shift", 20), (3, 12, False, "shift", 30),
+                                                    (6, 8, True, "symmetric_shift", 12),
+                                                    (5, 12, True, "symmetric_shift", 14),
+                                                    (16, 16, True, "symmetric_shift", 30)])   # a tie: k = 2 on 28
+def test_split_choice_is_best_simulated(BH, n, causal, mode, P_max):
+    # shift_split = -1: every k dividing the gang on its four largest candidate CTA counts (multiples of
+    # the sub-gang; symmetric shift also P_max itself), each simulated by the oracle; smallest makespan,
+    # ties to fewer CTAs within a k, then across k to a sub-gang that divides its CTA count, then to the
+    # smaller k
+    gang = n // 2 if causal else n
+    top = min(P_max, BH * gang)
+    best = None
+    for k in [k for k in range(1, gang + 1) if gang % k == 0]:
+        g = gang // k
+        cands = [] if mode == "shift" else [top]
+        m = (top // g) * g
+        while m >= g and len(cands) < 4:
+            if mode == "shift" or m != top:
+                cands.append(m)
+            m -= g
+        spans = []
+        for P in cands:
+            try:
+                spans.append((d.simulate(d.split_chains(mode, BH, n, causal, k), P, 4, 1).makespan, P))
+            except d.Deadlock:
+                continue
+        if spans:
+            ms, P = min(spans)
+            key = (ms, P % g != 0, k)
+            if best is None or key < best[0]:
+                best = (key, P)
+    k, P, ms = dash.dash_choose_split(BH, n, causal, mode, P_max)
+    assert (ms, P % ((n // 2 if causal else n) // k) != 0, k) == best[0] and P == best[1]
+    # on a given CTA count, shift only takes the k whose sub-gang divides it
+    k2, P2, _ = dash.dash_choose_split(BH, n, causal, mode, P_max, num_ctas=P_max)
+    assert P2 == P_max and (mode != "shift" or P_max % (gang // k2) == 0)
+    assert dash.dash_choose_split(BH, n, causal, "serial", P_max)[0] == -1
+

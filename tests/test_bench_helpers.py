@@ -34,6 +34,10 @@ def test_split_of_needs_a_divisor_of_the_gang():
     assert bench.split_of(full, "shift", 1) == 0             # 1 = whole gangs, not timed as an extension
     assert bench.split_of(full, "serial", 4) == 0
     assert bench.split_of(full, "symmetric_shift", 4) == 0   # not a schedule of the full mask
+    assert bench.split_of(full, "shift", -1) == -1           # the library's choice
+    assert bench.split_of(full, "serial", -1) == 0
+    assert bench.split_chosen(dash, full, "shift", -1, 152) == dash.dash_choose_split(32, 32, False, "shift", 152)[0]
+    assert bench.split_chosen(dash, full, "shift", 4, 152) == 4
     n = causal.S // causal.tile
     assert bench.split_of(causal, "symmetric_shift", 4) == (4 if (n // 2) % 4 == 0 else 0)
 

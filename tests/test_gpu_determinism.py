@@ -77,6 +77,30 @@ def test_two_dq_chains_bit_identical_across_runs(wname):
                      rel=2e-3, abs_=1e-2)
 
 
+SPLIT_WL = [w for w in WL if w.S >= 4096]
+
+
+@pytest.mark.parametrize("w", SPLIT_WL, ids=[w.name for w in SPLIT_WL])
+def test_split_gangs_bit_identical_across_runs(w):
+    # split gangs as the library picks them (an extension): a fixed (sub-gang, step) order per tile
+    sched = "symmetric_shift" if w.causal else "shift"
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    first = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, dq_accum=True, tile=w.tile,
+                          shift_split=-1)
+    outs = [torch.empty_like(x) for x in first]
+    same = True
+    for _ in range(RUNS - 1):
+        dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, outs[0], outs[1], outs[2], w.causal, P.scale,
+                              sched, tile=w.tile, dq_accum_out=outs[3], shift_split=-1)
+        same = same and all(torch.equal(a, b) for a, b in zip(outs, first))
+    dash.dash_sync_status()
+    assert same, f"{w.name}: {sched} with split gangs is not bit-identical across {RUNS} runs"
+    # dK and dV do not depend on the dQ order
+    one = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile)
+    assert torch.equal(one[1], first[1]) and torch.equal(one[2], first[2])
+
+
 def test_deterministic_schedules_agree_within_tolerance():
     # different schedules reduce dQ in different orders: close, not equal bits
     w = workloads.WORKLOADS["causal_s2048_d128"]

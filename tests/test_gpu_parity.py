@@ -183,24 +183,30 @@ def test_split_gangs_match_oracle(S, D, tile, causal, sched, split):
 
 @pytest.mark.parametrize("wname,sched", [("full_s4096_d128", "shift"), ("causal_s8192_d64", "symmetric_shift")])
 def test_split_gangs_full_size(wname, sched):
-    # split gangs of four at full size, on the CTA count the library picks:
-    # sampled rows of the first and last heads against the row-wise oracle,
-    # and the same bits on a second run
+    # split gangs at full size as the library picks them (shift_split = -1):
+    # the same bits as the chosen split asked for by name, and on a second
+    # run; sampled rows of the first and last heads against the row-wise oracle
     w = workloads.WORKLOADS[wname]
     BH = w.B * w.H
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    k, ctas, _ = dash.dash_choose_split(BH, w.S // w.tile, w.causal, sched, sms)
+    assert k >= 1
     P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
-    run = lambda: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile, shift_split=4)
-    got, again = run(), run()
+    run = lambda kk, **kw: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile,
+                                         shift_split=kk, **kw)
+    got, again, named = run(-1), run(-1), run(k, num_ctas=ctas)
     dash.dash_sync_status()
     assert all(torch.equal(a, b) for a, b in zip(got, again))
+    assert all(torch.equal(a, b) for a, b in zip(got, named))
+    print(f"{wname} {sched}: split {k} on {ctas} CTAs")
     q, k, v, do = P.f64
     rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1})
     for b_, h_ in ((0, 0), (w.B - 1, w.H - 1)):
         oh, lh = o[b_, h_].double().cpu().numpy(), lse[b_, h_].double().cpu().numpy()
         ref = A.backward_rows(q[b_, h_], k[b_, h_], v[b_, h_], oh, do[b_, h_], lh, w.causal, P.scale, rows)
         for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
-            assert_close(f"{sched} split 4 {name}[{b_},{h_}] rows", x[b_, h_][rows], r)
+            assert_close(f"{sched} split {k} {name}[{b_},{h_}] rows", x[b_, h_][rows], r)
 
 
 def _red_add_f32(acc, x):
