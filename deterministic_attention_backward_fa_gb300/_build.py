@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if log.strip():
                 print(log)
     tmp = LIB + ".tmp"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -32,11 +32,13 @@
 #include "schedule.h"
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <string>
 #include <cmath>
 #include <functional>
 #include <queue>
+#include <thread>
 #include <utility>
 
 namespace dash {
@@ -353,15 +355,32 @@ int choose_split(int BH, int n, bool causal, int mode, int P_max, int c, int r, 
   if (mode != kShift && mode != kSymmetricShift) return -1;
   if (!check_mode(mode, n, causal).empty() || BH < 1 || P_max < 1 || c < 1 || r < 1) return -1;
   const int gang = chains_per_head(mode, n);
+  std::vector<int> ks;
+  for (int k = 1; k <= gang; ++k)
+    if (gang % k == 0) ks.push_back(k);
+  // Each k is simulated on its own host thread (the simulations share nothing).
+  // Whole gangs (k = 1) take choose_ctas' own candidates; a split gang the two
+  // largest only: its closed form has no waits, so fewer CTAs only lose SMs.
+  std::vector<int> Ps(ks.size(), -1);
+  std::vector<long long> spans(ks.size(), 0);
+  auto run = [&](size_t i) {
+    Ps[i] = best_ctas(BH, n, causal, mode, P_max, c, r, ks[i], fixed_P, ks[i] == 1 ? 16 : 2, &spans[i]);
+  };
+  const size_t workers = std::min<size_t>(ks.size(), std::max(1u, std::thread::hardware_concurrency()));
+  std::vector<std::thread> pool;
+  std::atomic<size_t> next{0};
+  for (size_t w = 1; w < workers; ++w)
+    pool.emplace_back([&] {
+      for (size_t i; (i = next.fetch_add(1)) < ks.size();) run(i);
+    });
+  for (size_t i; (i = next.fetch_add(1)) < ks.size();) run(i);
+  for (auto &th : pool) th.join();
   int best_k = -1, best_P = 0;
   bool best_whole = false;
   long long best_ms = 0;
-  for (int k = 1; k <= gang; ++k) {
-    if (gang % k) continue;
-    long long ms = 0;
-    // the four largest candidate counts of each k: a split gang's closed form
-    // has no waits, so fewer CTAs only lose SMs
-    const int P = best_ctas(BH, n, causal, mode, P_max, c, r, k, fixed_P, 4, &ms);
+  for (size_t i = 0; i < ks.size(); ++i) {
+    const int k = ks[i], P = Ps[i];
+    const long long ms = spans[i];
     if (P < 1) continue;
     // On a tie, sub-gangs that fill the CTAs side by side win: a sub-gang
     // spread over time waits on its neighbours' hops, which the task costs

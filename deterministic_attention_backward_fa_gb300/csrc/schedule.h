@@ -50,8 +50,9 @@ std::string check_split(int mode, int n, int split);
 int choose_ctas(int BH, int n, bool causal, int mode, int P_max, int c, int r, int split = 1);
 
 // Split gangs chosen by simulation (shift and symmetric shift): every split k
-// that divides the gang, each on the best of choose_ctas' four largest
-// candidate CTA counts (or on fixed_P CTAs when fixed_P > 0; for shift only
+// that divides the gang, k = 1 on choose_ctas' CTA count and k > 1 on the
+// better of its two largest candidate counts (or on fixed_P CTAs when
+// fixed_P > 0; for shift only
 // where fixed_P is a multiple of the sub-gang), and the k of the smallest
 // simulated makespan; ties go first to a k whose sub-gang divides its CTA
 // count, then to the smaller k (so 1, whole gangs, wins a plain tie).

@@ -315,7 +315,8 @@ int dash_choose_split_ctas(int BH, int n, int causal, dash_schedule_t schedule, 
 
 /* The split that shift_split = -1 picks (an extension): for shift and
  * symmetric shift, every k that divides the gang (n, or n/2 for symmetric
- * shift), each on its dash_choose_split_ctas CTA count (on num_ctas CTAs when
+ * shift): k = 1 on the dash_choose_ctas count, k > 1 on the better of the two
+ * largest candidates of dash_choose_split_ctas (on num_ctas CTAs when
  * num_ctas > 0), and the k whose simulated makespan is smallest; ties go
  * first to a k whose sub-gang divides its CTA count (sub-gangs side by side,
  * none spread over time), then to the smaller k (1 = whole gangs).  Writes

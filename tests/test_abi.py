@@ -322,10 +322,10 @@ def test_split_rejections_and_cta_choice():
                                                     (5, 12, True, "symmetric_shift", 14),
                                                     (16, 16, True, "symmetric_shift", 30)])   # a tie: k = 2 on 28
 def test_split_choice_is_best_simulated(BH, n, causal, mode, P_max):
-    # shift_split = -1: every k dividing the gang on its four largest candidate CTA counts (multiples of
-    # the sub-gang; symmetric shift also P_max itself), each simulated by the oracle; smallest makespan,
-    # ties to fewer CTAs within a k, then across k to a sub-gang that divides its CTA count, then to the
-    # smaller k
+    # shift_split = -1: every k dividing the gang, k = 1 on up to sixteen candidate CTA counts and k > 1 on
+    # its two largest (multiples of the sub-gang; symmetric shift also P_max itself), each simulated by the
+    # oracle; smallest makespan, ties to fewer CTAs within a k, then across k to a sub-gang that divides its
+    # CTA count, then to the smaller k
     gang = n // 2 if causal else n
     top = min(P_max, BH * gang)
     best = None
@@ -333,7 +333,7 @@ def test_split_choice_is_best_simulated(BH, n, causal, mode, P_max):
         g = gang // k
         cands = [] if mode == "shift" else [top]
         m = (top // g) * g
-        while m >= g and len(cands) < 4:
+        while m >= g and len(cands) < (16 if k == 1 else 2):
             if mode == "shift" or m != top:
                 cands.append(m)
             m -= g

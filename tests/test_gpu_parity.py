@@ -209,6 +209,32 @@ def test_split_gangs_full_size(wname, sched):
             assert_close(f"{sched} split {k} {name}[{b_},{h_}] rows", x[b_, h_][rows], r)
 
 
+def test_split_gangs_run_shift_past_the_sm_count():
+    # a shift gang of n = 256 chains is larger than the GPU: whole gangs cannot
+    # run it (no CTA count holds one), split gangs can; sampled rows against
+    # the row-wise oracle, and the same bits twice
+    S, D = 32768, 64
+    n = S // 128
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert n > sms and dash.dash_choose_ctas(1, n, False, "shift", sms) == -1
+    P = Problem(1, 1, S, D, False)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, False, P.scale)
+    with pytest.raises(dash.DashError):
+        dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, False, P.scale, "shift")
+    k, ctas, _ = dash.dash_choose_split(1, n, False, "shift", sms)
+    assert k > 1 and ctas % (n // k) == 0
+    got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, False, P.scale, "shift", shift_split=-1)
+    again = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, False, P.scale, "shift", shift_split=-1)
+    dash.dash_sync_status()
+    assert all(torch.equal(a, b) for a, b in zip(got, again))
+    q, k_, v, do = P.f64
+    rows = [0, 127, 128, S // 2 + 5, S - 1]
+    ref = A.backward_rows(q[0, 0], k_[0, 0], v[0, 0], o[0, 0].double().cpu().numpy(), do[0, 0],
+                          lse[0, 0].double().cpu().numpy(), False, P.scale, rows)
+    for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+        assert_close(f"shift split {k} at n = {n} {name} rows", x[0, 0][rows], r)
+
+
 def _red_add_f32(acc, x):
     """fp32 add as red.global.add.f32 performs it: round to nearest even, with
     subnormal inputs and results flushed to (signed) zero."""
