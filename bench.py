@@ -265,14 +265,31 @@ def best_with_extensions(results, two_chains, fill, best, world, peak, die=None,
             "pct_bf16_peak": 100.0 * r["tflops"] / world / peak}
 
 
-def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best):
+def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best, measured_best_split=None):
     """The library's runtime schedule choice with task costs fitted to this run's atomic and
-    serial times, against the schedule measured best."""
+    serial times, against the schedule measured best; with `measured_best_split` (the best of the
+    pages' schedules and split gangs, e.g. "shift+split"), also the split-aware choice against it."""
     BH, n = w.B * w.H, w.S // w.tile
     c, r = dash.dash_fit_costs(BH, n, w.causal, sms, atomic_ms, serial_ms)
     chosen, ctas, _ = dash.dash_choose_schedule(BH, n, w.causal, sms, c, r)
-    return {"cost_c": c, "cost_r": r, "chosen": chosen, "ctas": ctas, "measured_best": measured_best,
-            "agrees": chosen == measured_best}
+    out = {"cost_c": c, "cost_r": r, "chosen": chosen, "ctas": ctas, "measured_best": measured_best,
+           "agrees": chosen == measured_best}
+    if measured_best_split is not None:
+        name, ctas_s, k, _ = dash.dash_choose_schedule_split(BH, n, w.causal, sms, c, r)
+        label = f"{name}+split" if k > 1 else name
+        out["with_split"] = {"chosen": label, "split": k, "ctas": ctas_s, "measured_best": measured_best_split,
+                             "agrees": label == measured_best_split}
+    return out
+
+
+def best_label(det, split):
+    """The fastest of the pages' schedules (TFLOPS by name) and the split-gang runs, split gangs labelled
+    "<schedule>+split" where they were timed with a split above one."""
+    cands = dict(det)
+    for s_, (t, k) in split.items():
+        if k > 1:
+            cands[f"{s_}+split"] = t
+    return max(cands, key=cands.get)
 
 
 def run_sweep(args, dash):
@@ -313,14 +330,15 @@ def run_sweep(args, dash):
         det = {s: t for s, t in res.items() if s != "atomic"}
         best = max(det, key=det.get)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        choice = runtime_choice(dash, w, sms, 1.0 / res["atomic"], 1.0 / res["serial"], best)
+        ks = {s_: split_chosen(dash, w, s_, args.split, sms) for s_ in split}
+        choice = runtime_choice(dash, w, sms, 1.0 / res["atomic"], 1.0 / res["serial"], best,
+                                best_label(det, {s_: (t, ks[s_]) for s_, t in split.items()}))
         print(json.dumps({"sweep": "pages_16k_tokens", "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
                           "mask": "causal" if w.causal else "full", "tile": w.tile, "unit": "TFLOPS",
                           "statistic": f"median of {args.steps} steps", "schedules": res,
                           "best_deterministic": best, "pct_bf16_peak": 100.0 * det[best] / peak,
                           "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
-                          "extension_split": {s: {"tflops": t, "vs_atomic": t / res["atomic"],
-                                                  "split": split_chosen(dash, w, s, args.split, sms)}
+                          "extension_split": {s: {"tflops": t, "vs_atomic": t / res["atomic"], "split": ks[s]}
                                               for s, t in split.items()} or None,
                           "runtime_choice": choice, "clocks": clk.summary()}), flush=True)
         del q, k_, v, do, o, lse, dq, dk, dv
@@ -489,7 +507,9 @@ def main():
     choice = None
     if atomic and "serial" in results:
         choice = runtime_choice(dash, w, torch.cuda.get_device_properties(dev).multi_processor_count,
-                                atomic["main_ms"], results["serial"]["main_ms"], best)
+                                atomic["main_ms"], results["serial"]["main_ms"], best,
+                                best_label({s_: r["tflops"] for s_, r in det.items()},
+                                           {s_: (r["tflops"], r["split"]) for s_, r in split.items()}))
 
     # end to end through the host-buffer entry point: H2D inputs, backward, D2H gradients
     pin = [t.pin_memory() for t in host] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]

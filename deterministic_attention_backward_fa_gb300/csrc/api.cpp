@@ -866,6 +866,21 @@ int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, in
   return s;
 }
 
+int dash_choose_schedule_split(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                               int *split_out, long long *makespan_out) {
+  int P = 0, split = 1;
+  long long ms = 0;
+  const int s = dash::choose_schedule(BH, n, causal != 0, max_ctas, cost_c, cost_r, &P, &ms, true, &split);
+  if (s < 0) {
+    dash::set_last_error("dash_choose_schedule_split: BH, n, max_ctas and the costs must be >= 1");
+    return -1;
+  }
+  if (ctas_out) *ctas_out = P;
+  if (split_out) *split_out = split;
+  if (makespan_out) *makespan_out = ms;
+  return s;
+}
+
 dash_status_t dash_cluster_latencies(const uint32_t *lat, int n_sms, int n_lines, int32_t *group_out,
                                      int32_t *home_out) {
   if (!lat || !group_out || !home_out || n_sms < 2 || n_lines < 1)

@@ -606,26 +606,37 @@ std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, d
   return "";
 }
 
-int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out) {
+int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out,
+                    bool allow_split, int *split_out) {
   if (BH < 1 || n < 1 || P_max < 1 || c < 1 || r < 1) return -1;
-  int best = -1, best_P = 0;
+  int best = -1, best_P = 0, best_split = 1;
   long long best_ms = 0;
   for (int mode : {kSerial, kDescendingQ, kShift, kSymmetricShift}) {
     if (!check_mode(mode, n, causal).empty()) continue;
-    const int P = choose_ctas(BH, n, causal, mode, P_max, c, r);
-    if (P < 1) continue;
-    const HeadPlan hp = head_plan(mode, n, causal);
-    const SimResult sim = simulate(hp, head_pred(hp, n), BH, P, c, r, true);
-    if (sim.deadlock) continue;
-    if (best < 0 || sim.makespan < best_ms) {  // ties keep the lower schedule number
+    int P = 0, split = 1;
+    long long ms = 0;
+    if (allow_split && (mode == kShift || mode == kSymmetricShift)) {
+      split = choose_split(BH, n, causal, mode, P_max, c, r, 0, &P, &ms);
+      if (split < 1) continue;
+    } else {
+      P = choose_ctas(BH, n, causal, mode, P_max, c, r);
+      if (P < 1) continue;
+      const HeadPlan hp = head_plan(mode, n, causal);
+      const SimResult sim = simulate(hp, head_pred(hp, n), BH, P, c, r, true);
+      if (sim.deadlock) continue;
+      ms = sim.makespan;
+    }
+    if (best < 0 || ms < best_ms) {  // ties keep the lower schedule number
       best = mode;
       best_P = P;
-      best_ms = sim.makespan;
+      best_ms = ms;
+      best_split = split;
     }
   }
   if (best >= 0) {
     if (P_out) *P_out = best_P;
     if (makespan_out) *makespan_out = best_ms;
+    if (split_out) *split_out = best_split;
   }
   return best;
 }

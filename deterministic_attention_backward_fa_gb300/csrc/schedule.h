@@ -110,7 +110,11 @@ std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, d
 
 // The deterministic schedule valid for the mask whose simulated makespan,
 // each at its own choose_ctas CTA count, is smallest (ties to the lower mode
-// number); fills its CTA count and makespan.  -1 on invalid arguments.
-int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out);
+// number); fills its CTA count and makespan.  With allow_split, shift and
+// symmetric shift enter with the split that choose_split picks (and its CTA
+// count), and split_out receives it (1 for the other schedules).  -1 on
+// invalid arguments.
+int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out,
+                    bool allow_split = false, int *split_out = nullptr);
 
 }  // namespace dash

@@ -347,6 +347,15 @@ int dash_choose_ctas(int BH, int n, int causal, dash_schedule_t schedule, int ma
 int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
                          long long *makespan_out);
 
+/* dash_choose_schedule with split gangs (an extension) among the candidates:
+ * shift or symmetric shift enters with the split and CTA count that
+ * dash_choose_split picks for it, so that its simulated makespan counts every
+ * SM it can use.  Writes the split as well (1 for serial, descending_q and
+ * whole gangs); a caller runs the result with dash_bwd_options_t.shift_split
+ * set to it (or -1) and num_ctas to the CTA count.  Same errors.  Host only. */
+int dash_choose_schedule_split(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                               int *split_out, long long *makespan_out);
+
 /* Task costs for dash_choose_schedule from measured times (the pages' DAG
  * model has a compute cost c and a reduce cost r per task; DASH overview
  * (zskr.cn), section 2.2).  Given the measured backward (or main-kernel)

@@ -147,6 +147,30 @@ def test_schedule_choice_is_best_simulated(BH, n, causal, c, r):
     assert dash.dash_choose_schedule(BH, n, causal, P_max, c, r) == (want, spans[want][1], best)
 
 
+@pytest.mark.parametrize("BH,n,causal,c,r", [(8, 4, False, 4, 1), (6, 8, True, 4, 1), (6, 8, True, 1, 3),
+                                             (3, 12, False, 2, 2), (16, 16, True, 4, 1)])
+def test_schedule_choice_with_split_gangs(BH, n, causal, c, r):
+    # the split-aware runtime choice: shift / symmetric shift enter with the split and CTA count that
+    # dash_choose_split picks (its makespan re-simulated by the oracle), the others as in dash_choose_schedule
+    P_max = 30
+    spans = {}
+    for mode in ("serial", "descending_q", "shift", "symmetric_shift"):
+        if (mode == "shift" and causal) or (mode == "symmetric_shift" and (not causal or n % 2)):
+            continue
+        if mode in ("shift", "symmetric_shift"):
+            k, P, ms = dash.dash_choose_split(BH, n, causal, mode, P_max, 0, c, r)
+            assert ms == d.simulate(d.split_chains(mode, BH, n, causal, k), P, c, r).makespan
+            spans[mode] = (ms, P, k)
+        else:
+            P = dash.dash_choose_ctas(BH, n, causal, mode, P_max, c, r)
+            spans[mode] = (d.simulate(d.all_chains(mode, BH, n, causal), P, c, r).makespan, P, 1)
+    best = min(s for s, _, _ in spans.values())
+    want = next(m for m in ("serial", "descending_q", "shift", "symmetric_shift") if m in spans and spans[m][0] == best)
+    assert dash.dash_choose_schedule_split(BH, n, causal, P_max, c, r) == (want, spans[want][1], spans[want][2], best)
+    # never worse than the choice without split gangs
+    assert best <= dash.dash_choose_schedule(BH, n, causal, P_max, c, r)[2]
+
+
 FILL_CASES = [("shift", False, 32, 32, 152), ("shift", False, 12, 16, 152), ("shift", False, 4, 32, 152),
               ("shift", False, 48, 16, 152), ("shift", False, 7, 4, 10), ("shift", False, 5, 3, 7),
               ("shift", False, 9, 6, 20), ("shift", False, 16, 8, 20), ("shift", False, 16, 128, 152),

@@ -42,6 +42,13 @@ def test_split_of_needs_a_divisor_of_the_gang():
     assert bench.split_of(causal, "symmetric_shift", 4) == (4 if (n // 2) % 4 == 0 else 0)
 
 
+def test_best_label_names_split_gangs_only_when_split():
+    det = {"serial": 600.0, "shift": 770.0}
+    assert bench.best_label(det, {"shift": (870.0, 4)}) == "shift+split"
+    assert bench.best_label(det, {"shift": (780.0, 1)}) == "shift"     # k = 1 is whole gangs: no label of its own
+    assert bench.best_label(det, {}) == "shift"
+
+
 def test_runtime_choice_uses_the_fitted_costs():
     import __graft_entry__
     __graft_entry__.build()
@@ -53,3 +60,6 @@ def test_runtime_choice_uses_the_fitted_costs():
     name, ctas, _ = dash.dash_choose_schedule(BH, n, w.causal, 152, c, r)
     assert (ch["chosen"], ch["ctas"]) == (name, ctas)
     assert ch["agrees"] == (name == "shift")
+    ch = bench.runtime_choice(dash, w, 152, 1.0, 1.45, "shift", "shift+split")
+    name, ctas, k, _ = dash.dash_choose_schedule_split(BH, n, w.causal, 152, c, r)
+    assert ch["with_split"]["chosen"] == (f"{name}+split" if k > 1 else name) and ch["with_split"]["split"] == k
