@@ -10,7 +10,8 @@ definition without forming an S x S matrix.  The rows are the first and last
 of the sequence, both sides of a tile boundary, one in the middle, and eight
 drawn from the seeded generator per configuration, so that tile-local errors
 away from those fixed rows are caught.  Every deterministic schedule must also
-give the same bits twice.
+give the same bits twice.  Shift or symmetric shift also runs with split gangs
+as the library picks them (an extension), to the same checks.
 """
 import numpy as np
 import pytest
@@ -52,14 +53,18 @@ def test_pages_sweep_sampled_rows(w):
         # the backward is fed the GPU's O and LSE, as the library's callers do
         oh, lh = o[b, h].double().cpu().numpy(), lse[b, h].double().cpu().numpy()
         refs[(b, h)] = A.backward_rows(qh, kh, vh, oh, doh, lh, w.causal, w.scale, rows)
-    for sched in w.schedules:
-        first = dash.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, sched, tile=w.tile)
+    # every schedule of the mask, and shift / symmetric shift with split gangs as the library picks them
+    runs = [(s_, 0) for s_ in w.schedules]
+    runs += [(s_, -1) for s_ in ("shift", "symmetric_shift") if s_ in w.schedules]
+    for sched, split in runs:
+        label = f"{sched} (split gangs)" if split else sched
+        first = dash.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, sched, tile=w.tile, shift_split=split)
         dash.dash_sync_status()
         for (b, h), ref in refs.items():
             for name, x, r in zip(("dQ", "dK", "dV"), first, ref):
-                assert_close(f"{w.name} {sched} {name}[{b},{h}] rows", x[b, h][rows], r)
+                assert_close(f"{w.name} {label} {name}[{b},{h}] rows", x[b, h][rows], r)
         assert all(torch.isfinite(x).all() for x in first)
         if sched != "atomic":
-            again = dash.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, sched, tile=w.tile)
+            again = dash.attn_bwd(q, k, v, o, do, lse, w.causal, w.scale, sched, tile=w.tile, shift_split=split)
             dash.dash_sync_status()
-            assert all(torch.equal(a, b) for a, b in zip(first, again)), f"{w.name} {sched} not bit-identical"
+            assert all(torch.equal(a, b) for a, b in zip(first, again)), f"{w.name} {label} not bit-identical"
