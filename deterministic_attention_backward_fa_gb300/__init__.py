@@ -46,7 +46,7 @@ class BwdOptions(ctypes.Structure):
                 ("main_begin_event", ctypes.c_void_p), ("main_end_event", ctypes.c_void_p),
                 ("dq_chains", ctypes.c_int), ("shift_fill", ctypes.c_int), ("trust_table", ctypes.c_int),
                 ("trace", ctypes.c_void_p), ("die_aware", ctypes.c_int), ("cluster_size", ctypes.c_int),
-                ("shift_split", ctypes.c_int)]
+                ("shift_split", ctypes.c_int), ("rank_order", ctypes.c_int)]
 
 # Slots of a trace row (dash_bwd_options_t.trace): see include/dash.h.
 TRACE_SLOTS = 21
@@ -70,6 +70,7 @@ _SIGS = {
                                           ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_ctas": ([_I] * 7, _I),
     "dash_build_split_schedule": ([_I] * 8 + [_P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
+    "dash_build_schedule_ex": ([_I] * 9 + [_P, _P, ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_split_ctas": ([_I] * 8, _I),
     "dash_choose_split": ([_I] * 8 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_schedule_split": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(_I),
@@ -169,7 +170,7 @@ def dash_attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, s
 def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float, schedule, tile=0,
                      num_ctas=0, cost_c=0, cost_r=0, spin_limit_ns=0, dq_accum_out=None, tasks=None,
                      cta_off=None, main_events=None, stream=None, dq_chains=0, shift_fill=0, trust_table=0,
-                     trace=None, die_aware=0, cluster_size=0, shift_split=0):
+                     trace=None, die_aware=0, cluster_size=0, shift_split=0, rank_order=0):
     """``main_events``: optional pair of recorded torch.cuda.Event objects (enable_timing) that the
     library records around the main kernel on the call's stream.  ``dq_chains=2`` splits each dQ
     tile's ordered reduction into two chains by rank parity; ``shift_fill=1`` runs some heads of a
@@ -179,7 +180,8 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     on one die with its semaphores homed there; ``cluster_size`` (0 or 1 = none; 2, 4, 8, 16) sets the thread-block
     clusters whose ranks hand the dQ turn over through shared memory; ``shift_split=k`` runs each gang of a
     shift or symmetric-shift schedule as k sub-gangs, and ``shift_split=-1`` lets the library pick k by
-    simulated makespan (see dash_bwd_options_t)."""
+    simulated makespan; ``rank_order=1`` reduces each dQ tile in the order the simulated schedule reaches
+    it (timed ranks; see dash_bwd_options_t)."""
     B, H, S, D = _shape(q)
     bf = torch.bfloat16
     opt = BwdOptions(tile, num_ctas, cost_c, cost_r, spin_limit_ns, None, None, None, None, None, dq_chains,
@@ -195,6 +197,7 @@ def dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal: bool, scale: float
     opt.die_aware = die_aware
     opt.cluster_size = cluster_size
     opt.shift_split = shift_split
+    opt.rank_order = rank_order
     if tasks is not None:
         t = np.ascontiguousarray(tasks, dtype=np.int32)
         o_ = np.ascontiguousarray(cta_off, dtype=np.int32)
@@ -281,6 +284,21 @@ def dash_fit_costs(BH: int, n: int, causal: bool, max_ctas: int, atomic_ms: floa
 
 def dash_choose_ctas(BH: int, n: int, causal: bool, schedule, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
     return int(lib().dash_choose_ctas(BH, n, int(causal), _sched(schedule), max_ctas, cost_c, cost_r))
+
+
+def dash_build_schedule_ex(BH: int, n: int, causal: bool, schedule, split: int, rank_order: int, P: int,
+                           cost_c: int = 4, cost_r: int = 1):
+    """Host-only tables with split gangs and / or timed ranks.  Returns (tasks int32 [N, 4], cta_off int32 [P+1],
+    makespan)."""
+    nt = dash_schedule_num_tasks(BH, n, causal, schedule)
+    if nt < 0:
+        raise DashError(2, "schedule invalid for this mask / n")
+    tasks = np.zeros((max(nt, 1), 4), dtype=np.int32)
+    off = np.zeros(P + 1, dtype=np.int32)
+    ms = ctypes.c_longlong(0)
+    _check(lib().dash_build_schedule_ex(BH, n, int(causal), _sched(schedule), split, rank_order, P, cost_c, cost_r,
+                                        tasks.ctypes.data, off.ctypes.data, ctypes.byref(ms)))
+    return tasks[:nt], off, ms.value
 
 
 def dash_build_split_schedule(BH: int, n: int, causal: bool, schedule, split: int, P: int, cost_c: int = 4,

@@ -343,6 +343,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
     why = dash::check_split(mode, n, split);
     if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
   }
+  if (opt && (opt->rank_order < 0 || opt->rank_order > 1)) return fail(DASH_ERR_INVALID_ARG, "rank_order must be 0 or 1");
+  const bool timed = opt && opt->rank_order == 1 && mode != DASH_SCHED_ATOMIC;
+  if (timed && (fill || opt->tasks || opt->die_aware == 1))
+    return fail(DASH_ERR_UNSUPPORTED, "rank_order = 1 applies to the library's own table, without fill or die_aware");
   if (opt && (opt->die_aware < 0 || opt->die_aware > 1)) return fail(DASH_ERR_INVALID_ARG, "die_aware must be 0 or 1");
   const bool die_aware = opt && opt->die_aware == 1;
   if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks || split > 1))
@@ -392,7 +396,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
     const int want = (opt && opt->num_ctas > 0) ? opt->num_ctas : 0;
     if (want > sms) return fail(DASH_ERR_UNSUPPORTED, "num_ctas %d exceeds the %d SMs", want, sms);
     auto key = std::make_tuple(dev, BH, n, causal ? 1 : 0, mode, want ? want : -sms, c, r, chains,
-                               fill ? -1 : split_auto ? -2 : split);
+                               (fill ? -1 : split_auto ? -2 : split) * 2 + (timed ? 1 : 0));
     auto &ent = g_sched[key];
     if (!ent) {
       std::unique_ptr<ScheduleEntry> fresh(new ScheduleEntry());
@@ -414,6 +418,10 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
       }
       if (!Puse && !fill && chains == 2 && mode == DASH_SCHED_SHIFT)
         Puse = (int)std::min<long long>(sms, (long long)BH * n);
+      // With timed ranks a gang spread over time does not stall (its tiles are
+      // reduced in the order the spread schedule reaches them): every SM.
+      if (!Puse && timed && use_split <= 1)
+        Puse = (int)std::min<long long>(sms, (long long)BH * dash::chains_per_head(mode, n));
       if (!Puse && !fill) Puse = dash::choose_ctas(BH, n, causal != 0, mode, sms, c, r, split);
       if (Puse < 1 && !fill) {
         g_sched.erase(key);
@@ -424,7 +432,7 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
         why = dash::build_fill(BH, n, causal != 0, mode, want ? want : sms, c, r, &sch, nullptr, nullptr);
         Puse = sch.P;
       } else {
-        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch, use_split);
+        why = dash::build_schedule(BH, n, causal != 0, mode, Puse, c, r, &sch, use_split, timed);
       }
       if (!why.empty()) {
         g_sched.erase(key);
@@ -808,6 +816,23 @@ dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t s
   if (ctas_out) *ctas_out = s.P;
   if (shift_heads_out) *shift_heads_out = hs;
   if (fill_schedule_out) *fill_schedule_out = fm;
+  if (makespan_out) *makespan_out = s.makespan;
+  return DASH_OK;
+}
+
+dash_status_t dash_build_schedule_ex(int BH, int n, int causal, dash_schedule_t schedule, int split, int rank_order,
+                                     int P, int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
+                                     long long *makespan_out) {
+  if (!tasks_out || !cta_off_out) return fail(DASH_ERR_INVALID_ARG, "null output pointer");
+  if (rank_order < 0 || rank_order > 1) return fail(DASH_ERR_INVALID_ARG, "rank_order must be 0 or 1");
+  std::string why = dash::check_mode((int)schedule, n, causal != 0);
+  if (why.empty()) why = dash::check_split((int)schedule, n, split);
+  if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
+  dash::Schedule s;
+  why = dash::build_schedule(BH, n, causal != 0, (int)schedule, P, cost_c, cost_r, &s, split, rank_order == 1);
+  if (!why.empty()) return fail(DASH_ERR_SCHEDULE, "%s", why.c_str());
+  std::memcpy(tasks_out, s.tasks.data(), s.tasks.size() * 4);
+  std::memcpy(cta_off_out, s.cta_off.data(), s.cta_off.size() * 4);
   if (makespan_out) *makespan_out = s.makespan;
   return DASH_OK;
 }

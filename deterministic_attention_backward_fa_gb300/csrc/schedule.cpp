@@ -39,6 +39,7 @@
 #include <functional>
 #include <queue>
 #include <thread>
+#include <tuple>
 #include <utility>
 
 namespace dash {
@@ -127,9 +128,13 @@ struct SimResult {
 };
 
 // order (optional): the global chain id (head * chains per head + chain) of
-// each dispatch, in dispatch order; identity when null.
+// each dispatch, in dispatch order; identity when null.  gpred (optional):
+// each task's predecessor as a global task id (head * tasks per head + task),
+// in place of the per-head hpred.  c_end (optional, sized BH * tasks per
+// head): receives the time each task's compute stage ends.
 SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, int P, int c, int r,
-                   bool ordered, const std::vector<long long> *order = nullptr) {
+                   bool ordered, const std::vector<long long> *order = nullptr,
+                   const std::vector<long long> *gpred = nullptr, std::vector<long long> *c_end = nullptr) {
   const int cph = (int)hp.off.size() - 1;   // chains per head
   const int tph = (int)hp.kv.size();        // tasks per head
   const long long nch = (long long)BH * cph;
@@ -181,8 +186,11 @@ SimResult simulate(const HeadPlan &hp, const std::vector<int> &hpred, int BH, in
       const int st = cta_step[s];
       const long long tid = task_id(ch, st);
       if (cta_phase[s] == 'C') {
+        if (c_end) (*c_end)[(size_t)tid] = T;
         long long p = -1;
-        if (ordered) {
+        if (ordered && gpred) {
+          p = (*gpred)[(size_t)tid];
+        } else if (ordered) {
           const int lp = hpred[(size_t)(tid % tph)];
           if (lp >= 0) p = (tid / tph) * tph + lp;
         }
@@ -235,6 +243,46 @@ std::vector<long long> split_order(int BH, int cph, int split) {
   return order;
 }
 
+// Timed ranks: each dQ tile's order is the order in which the simulated
+// schedule reaches it.  A run without reduction order gives every task's
+// compute end; the tasks of one (head, q) tile are ranked by that time, ties
+// by the dispatch position of their chain, then by step.  Fills the global
+// rank and predecessor of every task (head * tasks per head + task).
+void timed_ranks(const HeadPlan &hp, const std::vector<int> &hpred, int BH, int n, int P, int c, int r,
+                 const std::vector<long long> *order, std::vector<int> *rank, std::vector<long long> *gpred) {
+  const int cph = (int)hp.off.size() - 1, tph = (int)hp.kv.size();
+  const size_t nt = (size_t)BH * tph;
+  std::vector<long long> c_end(nt, 0);
+  simulate(hp, hpred, BH, P, c, r, false, order, nullptr, &c_end);
+  std::vector<long long> pos((size_t)BH * cph);
+  for (long long i = 0; i < (long long)pos.size(); ++i) pos[(size_t)(order ? (*order)[(size_t)i] : i)] = i;
+  std::vector<int> chain_of(tph), step_of(tph);
+  for (int ch = 0; ch < cph; ++ch)
+    for (int t = hp.off[ch]; t < hp.off[ch + 1]; ++t) {
+      chain_of[t] = ch;
+      step_of[t] = t - hp.off[ch];
+    }
+  rank->assign(nt, 0);
+  gpred->assign(nt, -1);
+  std::vector<std::vector<int>> by_q(n);
+  for (int t = 0; t < tph; ++t) by_q[hp.q[t]].push_back(t);
+  std::vector<std::tuple<long long, long long, int, long long>> keys;
+  for (int h = 0; h < BH; ++h) {
+    const long long base = (long long)h * tph;
+    for (int q = 0; q < n; ++q) {
+      keys.clear();
+      for (int t : by_q[q])
+        keys.emplace_back(c_end[(size_t)(base + t)], pos[(size_t)h * cph + chain_of[t]], step_of[t], base + t);
+      std::sort(keys.begin(), keys.end());
+      for (size_t i = 0; i < keys.size(); ++i) {
+        const long long tid = std::get<3>(keys[i]);
+        (*rank)[(size_t)tid] = (int)i;
+        if (i > 0) (*gpred)[(size_t)tid] = std::get<3>(keys[i - 1]);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 std::string check_split(int mode, int n, int split) {
@@ -262,7 +310,7 @@ long long num_tasks(int BH, int n, bool causal) {
 }
 
 std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
-                           Schedule *out, int split) {
+                           Schedule *out, int split, bool timed) {
   std::string e = check_mode(mode, n, causal);
   if (!e.empty()) return e;
   if (split < 1) split = 1;
@@ -272,9 +320,13 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
   const std::vector<int> hpred = head_pred(hp, n);
   const std::vector<long long> order = split > 1 ? split_order(BH, (int)hp.off.size() - 1, split)
                                                  : std::vector<long long>();
-  SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic, split > 1 ? &order : nullptr);
+  const std::vector<long long> *ord = split > 1 ? &order : nullptr;
+  std::vector<int> grank;
+  std::vector<long long> gpred;
+  if (timed && mode != kAtomic) timed_ranks(hp, hpred, BH, n, P, c, r, ord, &grank, &gpred);
+  SimResult sim = simulate(hp, hpred, BH, P, c, r, mode != kAtomic, ord, grank.empty() ? nullptr : &gpred);
   if (sim.deadlock) return "schedule simulation deadlocked (too few CTAs for the chain gang?)";
-  const int cph = (int)hp.off.size() - 1;
+  const int cph = (int)hp.off.size() - 1, tph = (int)hp.kv.size();
   out->tasks.clear();
   out->tasks.reserve((size_t)num_tasks(BH, n, causal) * 4);
   out->cta_off.assign(1, 0);
@@ -283,7 +335,7 @@ std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, i
       const int bh = ch / cph, lc = ch % cph;
       const int a = hp.off[lc], b = hp.off[lc + 1];
       for (int t = a; t < b; ++t) {
-        int32_t w = hp.rank[t];
+        int32_t w = grank.empty() ? hp.rank[t] : grank[(size_t)bh * tph + t];
         if (t == a || hp.kv[t - 1] != hp.kv[t]) w |= kTaskFirst;
         if (t == b - 1 || hp.kv[t + 1] != hp.kv[t]) w |= kTaskLast;
         out->tasks.push_back(bh);

@@ -39,8 +39,13 @@ long long num_tasks(int BH, int n, bool causal);
 // every head's sub-gang 0 first, then every head's sub-gang 1, and so on.  A
 // sub-gang keeps shift's property that no two of its chains reach one tile at
 // one step, and CTA counts that are multiples of the sub-gang become usable.
+// timed (the ordered schedules): each dQ tile's ranks follow the order in
+// which the simulated schedule reaches the tile (compute-stage end in a run
+// without reduction order; ties by the chain's dispatch position, then step)
+// instead of the schedule's own order.  Where the schedule runs as its order
+// assumes (whole shift gangs side by side) the two orders agree.
 std::string build_schedule(int BH, int n, bool causal, int mode, int P, int c, int r,
-                           Schedule *out, int split = 1);
+                           Schedule *out, int split = 1, bool timed = false);
 // "" when `split` is valid for the schedule and n, else why not.
 std::string check_split(int mode, int n, int split);
 

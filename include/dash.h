@@ -168,6 +168,16 @@ typedef struct {
                             * DASH_ERR_UNSUPPORTED otherwise, and with die_aware.  -1 = the library picks k
                             * by simulated makespan (dash_choose_split), where split gangs apply; with
                             * another schedule, fill, die_aware or a supplied table it means 0. */
+  int rank_order;          /* ordered schedules with the library's own table, without fill or die_aware (an
+                            * extension): 0 = each dQ tile's partials in the schedule's own order (the pages');
+                            * 1 = timed ranks: in the order in which the simulated schedule reaches the tile
+                            * (the compute-stage end of each task in a list-scheduling run without reduction
+                            * order, ties by the chain's dispatch position, then step).  Where the schedule
+                            * runs as its order assumes (whole shift gangs side by side, each tile visited
+                            * step by step) the two orders are the same bits; where it does not (a gang spread
+                            * over time, sub-gangs of one head side by side) timed ranks keep the order from
+                            * stalling.  Without a split or num_ctas the CTA count is then every SM (up to
+                            * the number of chains).  Deterministic, with its own bits. */
 } dash_bwd_options_t;
 
 /* Slots of a trace row.  "clk" = the SM's clock64, "ns" = the global timer.
@@ -306,6 +316,14 @@ dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t s
 dash_status_t dash_build_split_schedule(int BH, int n, int causal, dash_schedule_t schedule, int split, int P,
                                         int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
                                         long long *makespan_out);
+
+/* dash_build_schedule with both extensions of the order: `split` as
+ * dash_build_split_schedule (1 = whole gangs; shift and symmetric shift only
+ * above 1) and `rank_order` as dash_bwd_options_t.rank_order (0 = the
+ * schedule's own ranks, 1 = timed ranks).  Same sizes and errors; host only. */
+dash_status_t dash_build_schedule_ex(int BH, int n, int causal, dash_schedule_t schedule, int split, int rank_order,
+                                     int P, int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
+                                     long long *makespan_out);
 
 /* The CTA count the backward uses with split gangs when num_ctas = 0: the
  * multiple of the sub-gang up to max_ctas with the smallest simulated makespan

@@ -45,6 +45,10 @@ split_chains (an extension) is pinned by coverage, by each tile's ranks
 running sub-gang after sub-gang, by equality with the plain chains for a split
 of one, and by the closed form m * split * len * (c + r) with no wait on as
 many SMs as a sub-gang (the overview's optimal forms, section 3, per gang).
+timed_chains (an extension) is pinned by equality with the pages' ranks where
+whole shift gangs run side by side (the step order is then the time order), by
+ranks that are permutations of every tile's visits, and by a run that never
+waits longer than its own reduction order allows.
 """
 from __future__ import annotations
 
@@ -290,6 +294,32 @@ def split_chains(mode: str, BH: int, n: int, causal: bool, split: int):
 def split_tables(mode: str, BH: int, n: int, causal: bool, split: int, P: int, c: int = 4, r: int = 1):
     """``schedule_tables`` for split gangs (``split_chains``)."""
     return tables_of(split_chains(mode, BH, n, causal, split), P, c, r, ordered=True)
+
+
+def timed_chains(chains, P: int, c: int, r: int):
+    """Timed ranks (an extension beyond the pages' orders): every dQ tile is
+    reduced in the order in which the scheduled chains reach it.  The chains
+    (in dispatch order) are list-scheduled on P SMs without reduction order;
+    the visits of each (head, q) tile are ranked by the time their compute
+    stage ends, ties by the chain's dispatch position, then by step.  Returns
+    the chains with those ranks."""
+    sim = simulate(chains, P, c, r, ordered=False)
+    visits = {}
+    for ci, (bh, ch, _) in enumerate(chains):
+        for st, (kv, q) in enumerate(ch):
+            visits.setdefault((bh, q), []).append((sim.c_end[(ci, st)], ci, st))
+    rank = {}
+    for lst in visits.values():
+        for rk, (_, ci, st) in enumerate(sorted(lst)):
+            rank[(ci, st)] = rk
+    return [(bh, ch, [rank[(ci, st)] for st in range(len(ch))]) for ci, (bh, ch, _) in enumerate(chains)]
+
+
+def timed_tables(mode: str, BH: int, n: int, causal: bool, P: int, split: int = 1, c: int = 4, r: int = 1):
+    """``schedule_tables`` with timed ranks (``timed_chains``), of whole gangs
+    or of split gangs (``split_chains``)."""
+    chains = split_chains(mode, BH, n, causal, split) if split > 1 else all_chains(mode, BH, n, causal)
+    return tables_of(timed_chains(chains, P, c, r), P, c, r, ordered=True)
 
 
 def tables_of(chains, P: int, c: int, r: int, ordered: bool):

@@ -115,7 +115,10 @@ def test_error_codes_without_gpu():
     # (S = 1024, tile 128: a shift gang of 8 chains) are rejected before any CUDA call
     for fields, code, words in [({"shift_split": 3}, 2, "divide"), ({"shift_split": -2}, 1, "shift_split"),
                                 ({"shift_split": 2, "shift_fill": 1}, 2, "without fill"),
-                                ({"shift_split": 2, "die_aware": 1}, 2, "split gangs")]:
+                                ({"shift_split": 2, "die_aware": 1}, 2, "split gangs"),
+                                ({"rank_order": 2}, 1, "rank_order"),
+                                ({"rank_order": 1, "shift_fill": 1}, 2, "rank_order"),
+                                ({"rank_order": 1, "die_aware": 1}, 2, "rank_order")]:
         opt = dash.BwdOptions()
         for f, x in fields.items():
             setattr(opt, f, x)
@@ -378,4 +381,33 @@ def test_split_choice_is_best_simulated(BH, n, causal, mode, P_max):
     k2, P2, _ = dash.dash_choose_split(BH, n, causal, mode, P_max, num_ctas=P_max)
     assert P2 == P_max and (mode != "shift" or P_max % (gang // k2) == 0)
     assert dash.dash_choose_split(BH, n, causal, "serial", P_max)[0] == -1
+
+
+TIMED_CASES = [("shift", False, 3, 8, 1), ("shift", False, 5, 4, 1), ("shift", False, 3, 8, 2), ("shift", False, 2, 12, 2),
+               ("symmetric_shift", True, 3, 8, 1), ("symmetric_shift", True, 2, 12, 2), ("serial", False, 3, 8, 1),
+               ("serial", True, 5, 4, 1), ("descending_q", True, 2, 12, 1), ("atomic", False, 3, 8, 1)]
+
+
+@pytest.mark.parametrize("mode,causal,BH,n,split", TIMED_CASES)
+def test_timed_generator_matches_simulator(mode, causal, BH, n, split):
+    # timed ranks (an extension): the C++ tables equal the oracle twin's, whole or split gangs, on CTA counts
+    # that are and are not multiples of the gang; atomic keeps its own (unordered) table
+    for P in (3, 7, 10, 16, 40):
+        for c, r in ((4, 1), (2, 3)):
+            tasks, off, ms = dash.dash_build_schedule_ex(BH, n, causal, mode, split, 1, P, c, r)
+            if mode == "atomic":
+                py = d.schedule_tables(mode, BH, n, causal, P, c, r)
+            else:
+                py = d.timed_tables(mode, BH, n, causal, P, split, c, r)
+            assert np.array_equal(tasks, np.asarray(py[0], dtype=np.int32).reshape(-1, 4))
+            assert np.array_equal(off, np.asarray(py[1], dtype=np.int32)) and ms == py[2]
+
+
+def test_timed_ranks_rejections():
+    with pytest.raises(dash.DashError) as ei:
+        dash.dash_build_schedule_ex(2, 8, False, "shift", 1, 2, 8)
+    assert ei.value.code == 1
+    with pytest.raises(dash.DashError) as ei:   # a split of the serial schedule
+        dash.dash_build_schedule_ex(2, 8, False, "serial", 2, 1, 8)
+    assert ei.value.code == 2
 

@@ -229,3 +229,52 @@ def test_split_tables_of_one_equal_the_plain_tables():
         a = d.split_tables(mode, 3, n, causal, 1, P, 4, 1)
         b = d.schedule_tables(mode, 3, n, causal, P, 4, 1)
         assert a == b
+
+
+# ---- timed ranks (an extension beyond the pages' orders)
+
+@pytest.mark.parametrize("mode,causal,n,BH,P", [("shift", False, 8, 4, 8), ("shift", False, 8, 4, 16),
+                                                ("shift", False, 8, 4, 32), ("shift", False, 6, 3, 12),
+                                                ("symmetric_shift", True, 8, 4, 4), ("symmetric_shift", True, 8, 4, 12),
+                                                ("symmetric_shift", True, 16, 3, 16)])
+def test_timed_ranks_are_the_pages_ranks_for_whole_gangs_side_by_side(mode, causal, n, BH, P):
+    # whole gangs side by side (P a multiple of the gang) run in lockstep, so
+    # the order in which they reach a tile is its visiting-step order: the
+    # pages' ranks, bit for bit, and the same tables
+    chains = d.all_chains(mode, BH, n, causal)
+    timed = d.timed_chains(chains, P, 4, 1)
+    assert [rk for _, _, rk in timed] == [rk for _, _, rk in chains]
+    assert d.timed_tables(mode, BH, n, causal, P) == d.schedule_tables(mode, BH, n, causal, P)
+
+
+@pytest.mark.parametrize("mode,causal,n,BH,P,split", [("shift", False, 8, 5, 12, 1), ("shift", False, 8, 5, 12, 2),
+                                                      ("symmetric_shift", True, 16, 3, 10, 1),
+                                                      ("symmetric_shift", True, 16, 5, 12, 2),
+                                                      ("serial", False, 6, 4, 7, 1), ("descending_q", True, 8, 3, 9, 1)])
+@pytest.mark.parametrize("c,r", [(4, 1), (1, 3)])
+def test_timed_ranks_permute_each_tile_and_follow_the_schedule(mode, causal, n, BH, P, split, c, r):
+    base = d.split_chains(mode, BH, n, causal, split) if split > 1 else d.all_chains(mode, BH, n, causal)
+    timed = d.timed_chains(base, P, c, r)
+    # same chains and tasks, new ranks: each (head, q) tile's ranks are 0..k-1
+    assert [(bh, ch) for bh, ch, _ in timed] == [(bh, ch) for bh, ch, _ in base]
+    by_tile = {}
+    for bh, ch, rk in timed:
+        for (kv, q), x in zip(ch, rk):
+            by_tile.setdefault((bh, q), []).append(x)
+    assert all(sorted(v) == list(range(len(v))) for v in by_tile.values())
+    # the ranks follow the unordered run's compute ends, and the ordered run of
+    # the timed ranks completes (a deadlock raises) no later than the
+    # unordered run plus one reduction per task of the longest chain
+    free = d.simulate(base, P, c, r, ordered=False)
+    for ci, (bh, ch, rk) in enumerate(timed):
+        for st, ((kv, q), x) in enumerate(zip(ch, rk)):
+            for cj, (bh2, ch2, rk2) in enumerate(timed):
+                if bh2 != bh:
+                    continue
+                for st2, ((kv2, q2), x2) in enumerate(zip(ch2, rk2)):
+                    if q2 == q and x2 < x:
+                        assert (free.c_end[(cj, st2)], cj, st2) < (free.c_end[(ci, st)], ci, st)
+    ordered = d.simulate(timed, P, c, r)
+    longest = max(len(ch) for _, ch, _ in base)
+    assert ordered.makespan <= free.makespan + longest * r * BH
+

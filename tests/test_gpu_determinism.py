@@ -101,6 +101,25 @@ def test_split_gangs_bit_identical_across_runs(w):
     assert torch.equal(one[1], first[1]) and torch.equal(one[2], first[2])
 
 
+@pytest.mark.parametrize("wname,sched", [("causal_s16384_d128", "symmetric_shift"), ("full_s4096_d128", "shift"),
+                                         ("causal_s8192_d64", "symmetric_shift")])
+def test_timed_ranks_bit_identical_across_runs(wname, sched):
+    # timed ranks (an extension) on every SM: the order comes from a deterministic simulation, so the bits repeat
+    w = workloads.WORKLOADS[wname]
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    first = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, dq_accum=True, tile=w.tile,
+                          rank_order=1)
+    outs = [torch.empty_like(x) for x in first]
+    same = True
+    for _ in range(RUNS - 1):
+        dash.dash_attn_bwd_ex(P.q, P.k, P.v, o, P.do, lse, outs[0], outs[1], outs[2], w.causal, P.scale,
+                              sched, tile=w.tile, dq_accum_out=outs[3], rank_order=1)
+        same = same and all(torch.equal(a, b) for a, b in zip(outs, first))
+    dash.dash_sync_status()
+    assert same, f"{wname}: {sched} with timed ranks is not bit-identical across {RUNS} runs"
+
+
 def test_deterministic_schedules_agree_within_tolerance():
     # different schedules reduce dQ in different orders: close, not equal bits
     w = workloads.WORKLOADS["causal_s2048_d128"]

@@ -235,6 +235,55 @@ def test_split_gangs_run_shift_past_the_sm_count():
         assert_close(f"shift split {k} at n = {n} {name} rows", x[0, 0][rows], r)
 
 
+TIMED = [(512, 64, 64, False, 5), (500, 64, 64, False, 7), (1000, 64, 64, True, 9), (1024, 128, 128, True, 5),
+         (700, 128, 128, False, 4)]
+
+
+@pytest.mark.parametrize("S,D,tile,causal,ctas", TIMED, ids=[f"s{S}_d{D}_{'causal' if c else 'full'}_p{p}"
+                                                              for S, D, _, c, p in TIMED])
+def test_timed_ranks_match_oracle(S, D, tile, causal, ctas):
+    # timed ranks (an extension) for every ordered schedule of the mask, on the library's CTA count and on a
+    # count that spreads the gangs over time, with one and two dQ chains; the same bits on a second run
+    H = 3
+    P = Problem(1, H, S, D, causal)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
+    q, k, v, do = P.f64
+    ref = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    for sched in schedules_for(causal, S, tile):
+        if sched == "atomic":
+            continue
+        for chains in (1, 2):
+            for num in (0, ctas):
+                run = lambda: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile,
+                                            dq_chains=chains, rank_order=1, num_ctas=num)
+                got, again = run(), run()
+                dash.dash_sync_status()
+                for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+                    assert_close(f"{sched} timed, {chains} chain(s), {num} CTAs {name}", x, r)
+                assert all(torch.equal(a, b) for a, b in zip(got, again))
+
+
+@pytest.mark.parametrize("wname,sched", [("causal_s16384_d128", "symmetric_shift"), ("full_s4096_d128", "shift")])
+def test_timed_ranks_full_size(wname, sched):
+    # timed ranks on every SM at full size: sampled rows of the first and last heads against the row-wise oracle,
+    # the same bits twice; dK and dV equal the pages' order's (they do not depend on the dQ order)
+    w = workloads.WORKLOADS[wname]
+    P = Problem(w.B, w.H, w.S, w.D, w.causal, w.gain)
+    o, lse = dash.attn_fwd(P.q, P.k, P.v, w.causal, P.scale)
+    run = lambda **kw: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, w.causal, P.scale, sched, tile=w.tile, **kw)
+    got, again, plain = run(rank_order=1), run(rank_order=1), run()
+    dash.dash_sync_status()
+    assert all(torch.equal(a, b) for a, b in zip(got, again))
+    assert torch.equal(got[1], plain[1]) and torch.equal(got[2], plain[2])
+    q, k, v, do = P.f64
+    rows = sorted({0, w.tile - 1, w.tile, w.S // 2 + 5, w.S - 1})
+    for b_, h_ in ((0, 0), (w.B - 1, w.H - 1)):
+        oh, lh = o[b_, h_].double().cpu().numpy(), lse[b_, h_].double().cpu().numpy()
+        ref = A.backward_rows(q[b_, h_], k[b_, h_], v[b_, h_], oh, do[b_, h_], lh, w.causal, P.scale, rows)
+        for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+            assert_close(f"{sched} timed {name}[{b_},{h_}] rows", x[b_, h_][rows], r)
+
+
 def _red_add_f32(acc, x):
     """fp32 add as red.global.add.f32 performs it: round to nearest even, with
     subnormal inputs and results flushed to (signed) zero."""
@@ -272,22 +321,31 @@ def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
             dash.dash_sync_status()
             part[(bh, kv, q)] = acc.reshape(BH, S, D)[bh, q * tile:(q + 1) * tile].cpu().numpy()
     cyclic = "symmetric_shift" if causal else "shift"
-    # the pages' orders, and split gangs of two (an extension) for the cyclic schedule
-    for sched, split in (("serial", 1), ("descending_q", 1), (cyclic, 1), (cyclic, 2)):
-        if split == 1:
-            chains_ = d.head_chains(sched, n, causal)
-            ranked = zip(chains_, d.head_ranks(sched, n, causal, chains_))
+    # the pages' orders, split gangs of two (an extension) for the cyclic schedule, and timed ranks (an
+    # extension) of the cyclic schedule on 3 CTAs, which spreads its gangs over time (ranks per head)
+    for sched, split, timed in (("serial", 1, 0), ("descending_q", 1, 0), (cyclic, 1, 0), (cyclic, 2, 0),
+                                (cyclic, 1, 1)):
+        extra = {}
+        if timed:
+            tasks_t, _, _ = dash.dash_build_schedule_ex(BH, n, causal, sched, 1, 1, 3)
+            rank = {(int(b), int(kv), int(q)): int(w) & dash.TASK_RANK_MASK for b, kv, q, w in tasks_t}
+            extra = {"rank_order": 1, "num_ctas": 3}
         else:
-            ranked = [(ch, rks) for _, ch, rks in d.split_chains(sched, 1, n, causal, split)]
-        rank = {t: rk for ch, rks in ranked for t, rk in zip(ch, rks)}
+            if split == 1:
+                chains_ = d.head_chains(sched, n, causal)
+                ranked = zip(chains_, d.head_ranks(sched, n, causal, chains_))
+            else:
+                ranked = [(ch, rks) for _, ch, rks in d.split_chains(sched, 1, n, causal, split)]
+            head_rank = {t: rk for ch, rks in ranked for t, rk in zip(ch, rks)}
+            rank = {(bh, kv, q): head_rank[(kv, q)] for bh in range(BH) for kv, q in tiles}
         for nch in (1, 2):
             got = dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile, dq_accum=True,
-                                dq_chains=nch, shift_split=split)[3]
+                                dq_chains=nch, shift_split=split, **extra)[3]
             dash.dash_sync_status()
             got = got.reshape(BH, S, D).cpu().numpy()
             for bh in range(BH):
                 for q in range(n):
-                    order = sorted((rank[(kv, q)], kv) for kv, qq in tiles if qq == q)
+                    order = sorted((rank[(bh, kv, q)], kv) for kv, qq in tiles if qq == q)
                     sums = [None, None]
                     for rk, kv in order:
                         c = rk % nch
@@ -295,8 +353,8 @@ def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
                         sums[c] = x.copy() if sums[c] is None else _red_add_f32(sums[c], x)
                     want = sums[0] if nch == 1 or sums[1] is None else (sums[0] + sums[1]).astype(np.float32)
                     assert np.array_equal(got[bh, q * tile:(q + 1) * tile], want), \
-                        f"{sched} (split {split}), {nch} chain(s): head {bh}, dQ tile {q} differs from the " \
-                        "rank-order sum"
+                        f"{sched} (split {split}, timed {timed}), {nch} chain(s): head {bh}, dQ tile {q} differs " \
+                        "from the rank-order sum"
 
 
 LARGE = [w for w in workloads.WORKLOADS.values() if w.S >= 2048]
