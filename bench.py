@@ -15,8 +15,9 @@ chains leave idle run some heads in the serial or descending order), under
 each gang of chains on one die, its semaphores homed there) under
 `extension_die_aware`, and with split gangs (shift_split = -1: each head's gang
 runs as k sub-gangs, k picked by the library's simulation, so that the CTA
-count need only be a multiple of a sub-gang) under `extension_split`, never in
-`value`.  The long causal workload
+count need only be a multiple of a sub-gang) under `extension_split`, and with
+timed ranks (rank_order = 1: each dQ tile reduced in the order the scheduled
+chains reach it, on every SM) under `extension_timed`, never in `value`.  The long causal workload
 (causal_s16384_d128) is timed in the same run, every schedule of its mask and
 symmetric shift with fill, die-aware placement and split gangs, and reported
 under `workloads` with its own ratio
@@ -80,6 +81,8 @@ def parse():
     ap.add_argument("--split", type=int, default=-1,
                     help="split gangs timed for shift and symmetric shift (shift_split: -1 = the library's "
                          "choice, k > 1 = k sub-gangs, 0 or 1 skips)")
+    ap.add_argument("--no-timed", action="store_true",
+                    help="skip timing shift and symmetric shift with timed ranks (rank_order = 1)")
     ap.add_argument("--also", default="causal_s16384_d128",
                     help="comma-separated further workloads timed in the same run and reported under "
                          "`workloads` (every schedule of the mask and fill; '' for none)")
@@ -252,10 +255,11 @@ def split_chosen(dash, w, sched, k, sms):
     return dash.dash_choose_split(w.B * w.H, w.S // w.tile, w.causal, sched, sms)[0] if k == -1 else k
 
 
-def best_with_extensions(results, two_chains, fill, best, world, peak, die=None, split=None):
+def best_with_extensions(results, two_chains, fill, best, world, peak, die=None, split=None, timed=None):
     """The fastest deterministic layout including the extensions (never in `value`)."""
     cands = {best: results[best]}
     cands.update({f"{s}+split": r for s, r in (split or {}).items()})
+    cands.update({f"{s}+timed": r for s, r in (timed or {}).items()})
     cands.update({f"{s}+fill": r for s, r in fill.items()})
     cands.update({f"{s}+two_dq_chains": r for s, r in two_chains.items()})
     cands.update({f"{s}+die_aware": r for s, r in (die or {}).items()})
@@ -304,16 +308,18 @@ def run_sweep(args, dash):
         q, k_, v, do = (t.to(dev) for t in workloads.make_workload_inputs(w))
         o, lse = dash.attn_fwd(q, k_, v, w.causal, w.scale)
         dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-        res, fill, split = {}, {}, {}
-        runs = [(s, 0, 0) for s in w.schedules]
-        runs += [(s, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
-        runs += [(s, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift") if split_of(w, s, args.split)]
+        res, fill, split, timed = {}, {}, {}, {}
+        runs = [(s, 0, 0, 0) for s in w.schedules]
+        runs += [(s, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+        runs += [(s, 0, split_of(w, s, args.split), 0) for s in ("shift", "symmetric_shift")
+                 if split_of(w, s, args.split)]
+        runs += [(s, 0, 0, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_timed]
         with ClockSampler(0) as clk:
-            for sched, shift_fill, k in runs:
+            for sched, shift_fill, k, ro in runs:
                 for _ in range(args.warmup):
                     flush.fill_(1)
                     dash.dash_attn_bwd_ex(q, k_, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                          shift_fill=shift_fill, shift_split=k)
+                                          shift_fill=shift_fill, shift_split=k, rank_order=ro)
                 dash.dash_sync_status()
                 ms = []
                 for _ in range(args.steps):
@@ -321,12 +327,13 @@ def run_sweep(args, dash):
                     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     a.record(stream)
                     dash.dash_attn_bwd_ex(q, k_, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                          shift_fill=shift_fill, shift_split=k)
+                                          shift_fill=shift_fill, shift_split=k, rank_order=ro)
                     b.record(stream)
                     b.synchronize()
                     ms.append(a.elapsed_time(b))
                 dash.dash_sync_status()
-                (split if k else fill if shift_fill else res)[sched] = w.flops() / (statistics.median(ms) / 1e3) / 1e12
+                tf = w.flops() / (statistics.median(ms) / 1e3) / 1e12
+                (timed if ro else split if k else fill if shift_fill else res)[sched] = tf
         det = {s: t for s, t in res.items() if s != "atomic"}
         best = max(det, key=det.get)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -340,19 +347,22 @@ def run_sweep(args, dash):
                           "ratio_vs_atomic": det[best] / res["atomic"], "extension_fill": fill or None,
                           "extension_split": {s: {"tflops": t, "vs_atomic": t / res["atomic"], "split": ks[s]}
                                               for s, t in split.items()} or None,
+                          "extension_timed": {s: {"tflops": t, "vs_atomic": t / res["atomic"]}
+                                              for s, t in timed.items()} or None,
                           "runtime_choice": choice, "clocks": clk.summary()}), flush=True)
         del q, k_, v, do, o, lse, dq, dk, dv
         torch.cuda.empty_cache()
 
 
 def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
-    """Times each (schedule, dq_chains, shift_fill, die_aware, shift_split) of `runs`: W warm-up steps, then K steps, each
+    """Times each (schedule, dq_chains, shift_fill, die_aware, shift_split, rank_order) of `runs`: W warm-up steps,
+    then K steps, each
     bracketed by CUDA events on the launching stream, with the main kernel's own events inside."""
     q, k, v, o, do, lse, dq, dk, dv = tensors
     flops = w.flops()
-    results, two_chains, fill, die, split = {}, {}, {}, {}, {}
+    results, two_chains, fill, die, split, timed = {}, {}, {}, {}, {}, {}
     launches = 0
-    for sched, chains, shift_fill, die_aware, ks in runs:
+    for sched, chains, shift_fill, die_aware, ks, ro in runs:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                 torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
@@ -362,7 +372,8 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         for _ in range(args.warmup):
             flush.fill_(1)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
-                                  dq_chains=chains, shift_fill=shift_fill, die_aware=die_aware, shift_split=ks)
+                                  dq_chains=chains, shift_fill=shift_fill, die_aware=die_aware, shift_split=ks,
+                                  rank_order=ro)
         dash.dash_sync_status()
         barrier()
         torch.cuda.synchronize()
@@ -371,7 +382,7 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
             evs[i][0].record(stream)
             dash.dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, w.causal, w.scale, sched, tile=w.tile,
                                   main_events=(evs[i][1], evs[i][2]), dq_chains=chains,
-                                  shift_fill=shift_fill, die_aware=die_aware, shift_split=ks)
+                                  shift_fill=shift_fill, die_aware=die_aware, shift_split=ks, rank_order=ro)
             evs[i][3].record(stream)
         torch.cuda.synchronize()
         barrier()
@@ -380,13 +391,14 @@ def time_runs(dash, w, tensors, runs, args, flush, stream, world, dev, barrier):
         step_ms = [evs[i][0].elapsed_time(evs[i][3]) for i in range(args.steps)]
         main_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(args.steps)]
         total_s = max_over_ranks(sum(step_ms) / 1e3, world, dev)
-        out = split if ks else die if die_aware else fill if shift_fill else results if chains == 1 else two_chains
+        out = (timed if ro else split if ks else die if die_aware else fill if shift_fill else
+               results if chains == 1 else two_chains)
         out[sched] = {"ms": 1e3 * total_s / args.steps, "main_ms": statistics.mean(main_ms),
                       "tflops": whole_job_tflops(world, flops, args.steps, total_s)}
         if ks:
             sms = torch.cuda.get_device_properties(dev).multi_processor_count
             out[sched]["split"] = split_chosen(dash, w, sched, ks, sms)
-    return results, two_chains, fill, die, split, launches
+    return results, two_chains, fill, die, split, timed, launches
 
 
 def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
@@ -397,16 +409,19 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
     o, lse = dash.attn_fwd(q, k, v, w.causal, w.scale)
     dash.dash_sync_status()
     dq, dk, dv = (torch.empty_like(q) for _ in range(3))
-    runs = [(s, 1, 0, 0, 0) for s in w.schedules]
-    runs += [(s, 1, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
-    runs += [(s, 1, 0, 1, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_die_aware]
-    runs += [(s, 1, 0, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift") if split_of(w, s, args.split)]
-    results, _, fill, die, split, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
+    runs = [(s, 1, 0, 0, 0, 0) for s in w.schedules]
+    runs += [(s, 1, 1, 0, 0, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_die_aware]
+    runs += [(s, 1, 0, 0, split_of(w, s, args.split), 0) for s in ("shift", "symmetric_shift")
+             if split_of(w, s, args.split)]
+    runs += [(s, 1, 0, 0, 0, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_timed]
+    results, _, fill, die, split, timed, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
                                                 stream, world, dev, barrier)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     atomic = results["atomic"]
-    for r in list(results.values()) + list(fill.values()) + list(die.values()) + list(split.values()):
+    for r in (list(results.values()) + list(fill.values()) + list(die.values()) + list(split.values())
+              + list(timed.values())):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"]
     det = {s: r for s, r in results.items() if s != "atomic"}
     best = max(det, key=lambda s: det[s]["tflops"])
@@ -419,7 +434,8 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
            "extension_fill": fill or None,
            "extension_die_aware": die or None,
            "extension_split": split or None,
-           "best_with_extensions": best_with_extensions(results, {}, fill, best, world, peak, die, split),
+           "extension_timed": timed or None,
+           "best_with_extensions": best_with_extensions(results, {}, fill, best, world, peak, die, split, timed),
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                         "frac": achieved / peak, "kernel": "dash_bwd_main",
                         "peak_source": f"{peak_kind} bf16_tflops (burst)"},
@@ -482,14 +498,15 @@ def main():
             pass
 
     scheds = [s for s in w.schedules if not args.schedules or s in args.schedules.split(",")]
-    runs = [(s, 1, 0, 0, 0) for s in scheds]
-    runs += [(s, 2, 0, 0, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
-    runs += [(s, 1, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
-    runs += [(s, 1, 0, 1, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_die_aware]
-    runs += [(s, 1, 0, 0, split_of(w, s, args.split)) for s in ("shift", "symmetric_shift")
+    runs = [(s, 1, 0, 0, 0, 0) for s in scheds]
+    runs += [(s, 2, 0, 0, 0, 0) for s in scheds if s != "atomic" and not args.no_two_chains]
+    runs += [(s, 1, 1, 0, 0, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_shift_fill]
+    runs += [(s, 1, 0, 1, 0, 0) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_die_aware]
+    runs += [(s, 1, 0, 0, split_of(w, s, args.split), 0) for s in ("shift", "symmetric_shift")
              if s in scheds and split_of(w, s, args.split)]
+    runs += [(s, 1, 0, 0, 0, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_timed]
     with ClockSampler(gpu_index) as clk:
-        results, two_chains, fill, die, split, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
+        results, two_chains, fill, die, split, timed, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
                                                              args, flush, stream, world, dev, barrier)
         also = {}
         for name in [x for x in args.also.split(",") if x and x != w.name]:
@@ -502,7 +519,7 @@ def main():
     best = max(det, key=lambda s: det[s]["tflops"])
     atomic = results.get("atomic")
     for s, r in (list(results.items()) + list(two_chains.items()) + list(fill.items()) + list(die.items())
-                 + list(split.items())):
+                 + list(split.items()) + list(timed.items())):
         r["vs_atomic"] = r["tflops"] / atomic["tflops"] if atomic else None
     choice = None
     if atomic and "serial" in results:
@@ -553,7 +570,8 @@ def main():
                        "flops_per_step": flops},
             "pct_bf16_peak": 100.0 * results[best]["tflops"] / world / peak,
             "ratio_vs_atomic": results[best]["vs_atomic"],
-            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak, die, split),
+            "best_with_extensions": best_with_extensions(results, two_chains, fill, best, world, peak, die, split,
+                                                         timed),
             "schedules": results,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic, "kernel": "dash_bwd_main",
@@ -566,6 +584,7 @@ def main():
             "extension_die_aware": die or None,
             "extension_fill": fill or None,
             "extension_split": split or None,
+            "extension_timed": timed or None,
             "runtime_choice": choice,
             "gpu_launches": launches,
             "clocks": clocks,

@@ -25,6 +25,9 @@ def test_best_with_extensions_picks_the_fastest_layout():
     split = {"shift": {"tflops": 870.0, "vs_atomic": 0.967, "split": 4}}
     b = bench.best_with_extensions(res, two, fill, "shift", 1, 2000.0, split=split)
     assert b["schedule"] == "shift+split" and b["tflops"] == 870.0
+    timed = {"shift": {"tflops": 880.0, "vs_atomic": 0.978}}
+    b = bench.best_with_extensions(res, two, fill, "shift", 1, 2000.0, split=split, timed=timed)
+    assert b["schedule"] == "shift+timed" and b["tflops"] == 880.0
 
 
 def test_split_of_needs_a_divisor_of_the_gang():
