@@ -24,9 +24,9 @@ import sys
 import numpy as np
 import torch
 
-from . import (TRACE_SLOTS, attn_fwd, dash_attn_bwd_ex, dash_build_schedule, dash_build_shift_fill,
-               dash_build_split_schedule, dash_choose_ctas, dash_choose_split, dash_choose_split_ctas,
-               dash_sync_status)
+from . import (TRACE_SLOTS, attn_fwd, dash_attn_bwd_ex, dash_build_schedule, dash_build_schedule_ex,
+               dash_build_shift_fill, dash_build_split_schedule, dash_choose_ctas, dash_choose_split,
+               dash_choose_split_ctas, dash_sync_status)
 
 # slot indices (include/dash.h)
 MMA_DP, MMA_DV, MMA_DQ, MMA_END = 0, 1, 2, 3
@@ -37,12 +37,19 @@ PASS_A_LAST, PASS_B_LAST, MMA_DV_OUT, MMA_DS_SEEN = 17, 18, 19, 20
 L2_FLUSH_BYTES = 256 << 20
 
 
-def task_table(BH, n, causal, schedule, sms, fill=False, chains=1, split=1, ctas=0):
+def task_table(BH, n, causal, schedule, sms, fill=False, chains=1, split=1, ctas=0, timed=False):
     """The table the library would build for this call (same generator and CTA choice; `ctas`, if set,
-    is the CTA count asked for)."""
+    is the CTA count asked for; `timed`: rank_order = 1)."""
     if split == -1:   # the library's choice of split and CTA count
         split, P, _ = dash_choose_split(BH, n, causal, schedule, sms, ctas)
         ctas = ctas or P
+    if timed:
+        if split > 1:
+            P = ctas or dash_choose_split_ctas(BH, n, causal, schedule, split, sms)
+        else:
+            P = ctas or min(sms, BH * (n // 2 if schedule == "symmetric_shift" else n))
+        tasks, off, _ = dash_build_schedule_ex(BH, n, causal, schedule, max(split, 1), 1, P)
+        return tasks, off, P
     if split > 1:
         P = ctas or dash_choose_split_ctas(BH, n, causal, schedule, split, sms)
         tasks, off, _ = dash_build_split_schedule(BH, n, causal, schedule, split, P)
@@ -61,7 +68,7 @@ def task_table(BH, n, causal, schedule, sms, fill=False, chains=1, split=1, ctas
 
 
 def run(q, k, v, o, do, lse, causal, scale, schedule, tasks, off, tile=128, chains=1, steps=5, warmup=3,
-        die_aware=0, cluster_size=0, supply_table=False, split=0, ctas=0, fill=0):
+        die_aware=0, cluster_size=0, supply_table=False, split=0, ctas=0, fill=0, rank_order=0):
     """Times the main kernel plain and traced on the same table; returns (trace int64 [n_tasks,
     TRACE_SLOTS] of the last traced run, plain ms, traced ms, outputs equal).  The kernel runs the
     library's own table, which task_table reproduces (with its cluster hand-offs, or die-aware
@@ -84,6 +91,7 @@ def run(q, k, v, o, do, lse, causal, scale, schedule, tasks, off, tile=128, chai
             dash_attn_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, causal, scale, schedule, tile=tile,
                              main_events=(a, b), dq_chains=chains, trace=tr if traced else None,
                              die_aware=die_aware, cluster_size=cluster_size, shift_split=split, shift_fill=fill,
+                             rank_order=rank_order,
                              num_ctas=0 if supply_table else ctas, **table)
             b.synchronize()
             if i >= warmup:
@@ -181,6 +189,7 @@ def main(argv=None):
     ap.add_argument("--split", type=int, default=0,
                     help="split gangs of shift and symmetric shift (shift_split; -1 = the library's choice)")
     ap.add_argument("--ctas", type=int, default=0, help="CTA count (num_ctas); 0 = the library's choice")
+    ap.add_argument("--timed", action="store_true", help="timed ranks (rank_order = 1)")
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--out", default="")
     args = ap.parse_args(argv)
@@ -194,17 +203,19 @@ def main(argv=None):
     dash_sync_status()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     BH, n = w.B * w.H, w.n_blocks
-    tasks, off, P = task_table(BH, n, w.causal, args.schedule, sms, args.fill, args.chains, args.split, args.ctas)
+    tasks, off, P = task_table(BH, n, w.causal, args.schedule, sms, args.fill, args.chains, args.split, args.ctas,
+                               args.timed)
     tr, plain_ms, traced_ms, same = run(q, k, v, o, do, lse, w.causal, w.scale, args.schedule, tasks, off,
                                         w.tile, args.chains, args.steps, die_aware=int(args.die_aware),
                                         cluster_size=args.cluster_size, split=args.split, ctas=args.ctas,
-                                        fill=int(args.fill))
+                                        fill=int(args.fill), rank_order=int(args.timed))
     rows, sm_mhz, viol, n_sms = summarize(tasks, off, tr, args.chains if args.schedule != "atomic" else 0)
     name = args.schedule + (" with fill" if args.fill else "") + (" two dQ chains" if args.chains == 2 else "")
     name += " die-aware" if args.die_aware else ""
     name += f", clusters of {args.cluster_size}" if args.cluster_size > 1 else ""
     name += (f", split gangs of {args.split}" if args.split > 1 else
              ", split gangs as the library picks them" if args.split == -1 else "")
+    name += ", timed ranks" if args.timed else ""
     cmd = " ".join(["python -m deterministic_attention_backward_fa_gb300.trace"] + (argv or sys.argv[1:]))
     lines = [f"# Phase trace of dash_bwd_main: {w.name}, {name}", "",
              f"Command: `{cmd}`", "",

@@ -25,22 +25,24 @@ def built():
     __graft_entry__.build()
 
 
-# S, D, mask, schedule, dQ chains, split gangs, fill, CTA count (0 = the library's choice)
-TRACED = [(512, 128, False, "shift", 1, 0, 0, 0), (512, 128, True, "symmetric_shift", 1, 0, 0, 0),
-          (1024, 64, True, "descending_q", 2, 0, 0, 0), (512, 128, False, "atomic", 1, 0, 0, 0),
-          (1024, 128, False, "shift", 1, 2, 0, 8), (1024, 64, True, "symmetric_shift", 2, 2, 0, 0),
-          (1024, 128, False, "shift", 1, 0, 1, 10)]
+# S, D, mask, schedule, dQ chains, split gangs, fill, CTA count (0 = the library's choice), timed ranks
+TRACED = [(512, 128, False, "shift", 1, 0, 0, 0, 0), (512, 128, True, "symmetric_shift", 1, 0, 0, 0, 0),
+          (1024, 64, True, "descending_q", 2, 0, 0, 0, 0), (512, 128, False, "atomic", 1, 0, 0, 0, 0),
+          (1024, 128, False, "shift", 1, 2, 0, 8, 0), (1024, 64, True, "symmetric_shift", 2, 2, 0, 0, 0),
+          (1024, 128, False, "shift", 1, 0, 1, 10, 0), (1024, 128, False, "shift", 1, 0, 0, 10, 1),
+          (2048, 64, True, "symmetric_shift", 1, 0, 0, 11, 1)]
 
 
-@pytest.mark.parametrize("S,D,causal,sched,chains,split,fill,ctas", TRACED)
-def test_trace_stamps_every_task_in_order(S, D, causal, sched, chains, split, fill, ctas):
+@pytest.mark.parametrize("S,D,causal,sched,chains,split,fill,ctas,timed", TRACED)
+def test_trace_stamps_every_task_in_order(S, D, causal, sched, chains, split, fill, ctas, timed):
     P = Problem(1, 3, S, D, causal)
     o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     BH, n = 3, S // 128
-    tasks, off, ctas = T.task_table(BH, n, causal, sched, sms, fill=bool(fill), chains=chains, split=split, ctas=ctas)
+    tasks, off, ctas = T.task_table(BH, n, causal, sched, sms, fill=bool(fill), chains=chains, split=split, ctas=ctas,
+                                    timed=bool(timed))
     tr, _, _, same = T.run(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tasks, off, 128, chains,
-                           steps=1, warmup=1, split=split, ctas=ctas, fill=fill)
+                           steps=1, warmup=1, split=split, ctas=ctas, fill=fill, rank_order=timed)
     if sched != "atomic":   # atomic adds land in no fixed order, so only the ordered schedules repeat bits
         assert same, "the traced kernel changed the results"
     assert (tr[:, [T.MMA_DP, T.MMA_DV, T.MMA_DQ, T.MMA_END, T.RED_Q, T.RED_LD, T.ACQ0, T.ACQ1, T.REL0,
