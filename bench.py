@@ -269,10 +269,12 @@ def best_with_extensions(results, two_chains, fill, best, world, peak, die=None,
             "pct_bf16_peak": 100.0 * r["tflops"] / world / peak}
 
 
-def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best, measured_best_split=None):
+def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best, measured_best_split=None,
+                   measured_best_layout=None):
     """The library's runtime schedule choice with task costs fitted to this run's atomic and
     serial times, against the schedule measured best; with `measured_best_split` (the best of the
-    pages' schedules and split gangs, e.g. "shift+split"), also the split-aware choice against it."""
+    pages' schedules and split gangs, e.g. "shift+split"), also the split-aware choice against it; with
+    `measured_best_layout` (the best of those and timed ranks), also dash_choose_layout against it."""
     BH, n = w.B * w.H, w.S // w.tile
     c, r = dash.dash_fit_costs(BH, n, w.causal, sms, atomic_ms, serial_ms)
     chosen, ctas, _ = dash.dash_choose_schedule(BH, n, w.causal, sms, c, r)
@@ -283,16 +285,23 @@ def runtime_choice(dash, w, sms, atomic_ms, serial_ms, measured_best, measured_b
         label = f"{name}+split" if k > 1 else name
         out["with_split"] = {"chosen": label, "split": k, "ctas": ctas_s, "measured_best": measured_best_split,
                              "agrees": label == measured_best_split}
+    if measured_best_layout is not None:
+        name, ctas_l, k, ro, _ = dash.dash_choose_layout(BH, n, w.causal, sms, c, r)
+        label = name + ("+split" if k > 1 else "") + ("+timed" if ro else "")
+        out["layout"] = {"chosen": label, "split": k, "rank_order": ro, "ctas": ctas_l,
+                         "measured_best": measured_best_layout, "agrees": label == measured_best_layout}
     return out
 
 
-def best_label(det, split):
-    """The fastest of the pages' schedules (TFLOPS by name) and the split-gang runs, split gangs labelled
-    "<schedule>+split" where they were timed with a split above one."""
+def best_label(det, split, timed=None):
+    """The fastest of the pages' schedules (TFLOPS by name), the split-gang runs and the timed-rank runs, split
+    gangs labelled "<schedule>+split" where they were timed with a split above one, timed ranks "<schedule>+timed"."""
     cands = dict(det)
     for s_, (t, k) in split.items():
         if k > 1:
             cands[f"{s_}+split"] = t
+    for s_, t in (timed or {}).items():
+        cands[f"{s_}+timed"] = t
     return max(cands, key=cands.get)
 
 
@@ -339,7 +348,8 @@ def run_sweep(args, dash):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         ks = {s_: split_chosen(dash, w, s_, args.split, sms) for s_ in split}
         choice = runtime_choice(dash, w, sms, 1.0 / res["atomic"], 1.0 / res["serial"], best,
-                                best_label(det, {s_: (t, ks[s_]) for s_, t in split.items()}))
+                                best_label(det, {s_: (t, ks[s_]) for s_, t in split.items()}),
+                                best_label(det, {s_: (t, ks[s_]) for s_, t in split.items()}, timed))
         print(json.dumps({"sweep": "pages_16k_tokens", "workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D,
                           "mask": "causal" if w.causal else "full", "tile": w.tile, "unit": "TFLOPS",
                           "statistic": f"median of {args.steps} steps", "schedules": res,
@@ -526,7 +536,10 @@ def main():
         choice = runtime_choice(dash, w, torch.cuda.get_device_properties(dev).multi_processor_count,
                                 atomic["main_ms"], results["serial"]["main_ms"], best,
                                 best_label({s_: r["tflops"] for s_, r in det.items()},
-                                           {s_: (r["tflops"], r["split"]) for s_, r in split.items()}))
+                                           {s_: (r["tflops"], r["split"]) for s_, r in split.items()}),
+                                best_label({s_: r["tflops"] for s_, r in det.items()},
+                                           {s_: (r["tflops"], r["split"]) for s_, r in split.items()},
+                                           {s_: r["tflops"] for s_, r in timed.items()}))
 
     # end to end through the host-buffer entry point: H2D inputs, backward, D2H gradients
     pin = [t.pin_memory() for t in host] + [o.cpu().pin_memory(), lse.cpu().pin_memory()]

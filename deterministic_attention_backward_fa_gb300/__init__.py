@@ -75,6 +75,7 @@ _SIGS = {
     "dash_choose_split": ([_I] * 8 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_choose_schedule_split": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(_I),
                                                ctypes.POINTER(ctypes.c_longlong)], _I),
+    "dash_choose_layout": ([_I] * 6 + [ctypes.POINTER(_I)] * 3 + [ctypes.POINTER(ctypes.c_longlong)], _I),
     "dash_check_table": ([_I] * 4 + [_P, _P, _I], _I),
     "dash_fit_costs": ([_I] * 4 + [ctypes.c_double] * 2 + [ctypes.POINTER(_I)] * 2, _I),
     "dash_choose_schedule": ([_I] * 6 + [ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_longlong)], _I),
@@ -339,6 +340,17 @@ def dash_choose_schedule_split(BH: int, n: int, causal: bool, max_ctas: int, cos
     if s < 0:
         raise DashError(1, dash_last_error())
     return {v: k_ for k_, v in SCHEDULES.items()}[s], P.value, k.value, ms.value
+
+
+def dash_choose_layout(BH: int, n: int, causal: bool, max_ctas: int, cost_c: int = 4, cost_r: int = 1):
+    """Host-only.  The runtime choice over every deterministic layout: returns (schedule name, CTA count, split,
+    rank_order, simulated makespan)."""
+    P, k, ro, ms = _I(0), _I(0), _I(0), ctypes.c_longlong(0)
+    s = lib().dash_choose_layout(BH, n, int(causal), max_ctas, cost_c, cost_r, ctypes.byref(P), ctypes.byref(k),
+                                 ctypes.byref(ro), ctypes.byref(ms))
+    if s < 0:
+        raise DashError(1, dash_last_error())
+    return {v: k_ for k_, v in SCHEDULES.items()}[s], P.value, k.value, ro.value, ms.value
 
 
 def dash_choose_schedule(BH: int, n: int, causal: bool, max_ctas: int, cost_c: int = 4, cost_r: int = 1):

@@ -820,6 +820,22 @@ dash_status_t dash_build_shift_fill(int BH, int n, int causal, dash_schedule_t s
   return DASH_OK;
 }
 
+int dash_choose_layout(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                       int *split_out, int *rank_order_out, long long *makespan_out) {
+  int P = 0, split = 1, timed = 0;
+  long long ms = 0;
+  const int s = dash::choose_layout(BH, n, causal != 0, max_ctas, cost_c, cost_r, &P, &split, &timed, &ms);
+  if (s < 0) {
+    dash::set_last_error("dash_choose_layout: BH, n, max_ctas and the costs must be >= 1");
+    return -1;
+  }
+  if (ctas_out) *ctas_out = P;
+  if (split_out) *split_out = split;
+  if (rank_order_out) *rank_order_out = timed;
+  if (makespan_out) *makespan_out = ms;
+  return s;
+}
+
 dash_status_t dash_build_schedule_ex(int BH, int n, int causal, dash_schedule_t schedule, int split, int rank_order,
                                      int P, int cost_c, int cost_r, int32_t *tasks_out, int32_t *cta_off_out,
                                      long long *makespan_out) {

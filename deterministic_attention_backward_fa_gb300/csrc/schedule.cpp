@@ -693,4 +693,45 @@ int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_
   return best;
 }
 
+int choose_layout(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, int *split_out, int *timed_out,
+                  long long *makespan_out) {
+  if (BH < 1 || n < 1 || P_max < 1 || c < 1 || r < 1) return -1;
+  int best = -1, best_P = 0, best_split = 1, best_timed = 0;
+  long long best_ms = 0;
+  auto consider = [&](int mode, int P, int split, int timed, long long ms) {
+    // ties keep the earlier candidate: the lower schedule number, then the
+    // pages' order before split gangs before timed ranks
+    if (best < 0 || ms < best_ms) {
+      best = mode;
+      best_P = P;
+      best_split = split;
+      best_timed = timed;
+      best_ms = ms;
+    }
+  };
+  for (int mode : {kSerial, kDescendingQ, kShift, kSymmetricShift}) {
+    if (!check_mode(mode, n, causal).empty()) continue;
+    const bool cyclic = mode == kShift || mode == kSymmetricShift;
+    const int P = choose_ctas(BH, n, causal, mode, P_max, c, r);
+    Schedule sch;
+    if (P >= 1 && build_schedule(BH, n, causal, mode, P, c, r, &sch).empty()) consider(mode, P, 1, 0, sch.makespan);
+    int Pk = 0;
+    long long msk = 0;
+    const int k = cyclic ? choose_split(BH, n, causal, mode, P_max, c, r, 0, &Pk, &msk) : 1;
+    if (cyclic && k > 1) consider(mode, Pk, k, 0, msk);
+    // timed ranks: whole gangs on every SM, and the chosen split's gangs
+    const int Pall = (int)std::min<long long>(P_max, (long long)BH * chains_per_head(mode, n));
+    if (build_schedule(BH, n, causal, mode, Pall, c, r, &sch, 1, true).empty()) consider(mode, Pall, 1, 1, sch.makespan);
+    if (cyclic && k > 1 && build_schedule(BH, n, causal, mode, Pk, c, r, &sch, k, true).empty())
+      consider(mode, Pk, k, 1, sch.makespan);
+  }
+  if (best >= 0) {
+    if (P_out) *P_out = best_P;
+    if (split_out) *split_out = best_split;
+    if (timed_out) *timed_out = best_timed;
+    if (makespan_out) *makespan_out = best_ms;
+  }
+  return best;
+}
+
 }  // namespace dash

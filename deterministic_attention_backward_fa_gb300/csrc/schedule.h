@@ -122,4 +122,14 @@ std::string fit_costs(int BH, int n, bool causal, int P_max, double atomic_ms, d
 int choose_schedule(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, long long *makespan_out,
                     bool allow_split = false, int *split_out = nullptr);
 
+// The deterministic layout with the smallest simulated makespan among every
+// ordered schedule valid for the mask in its own order (choose_ctas CTAs),
+// shift / symmetric shift with the split choose_split picks, and each of
+// those with timed ranks (whole gangs on every SM, split gangs on the split's
+// CTA count).  Ties keep the lower schedule number, then the own order before
+// split gangs before timed ranks.  Fills the CTA count, split (1 = whole
+// gangs) and timed flag; -1 on invalid arguments.
+int choose_layout(int BH, int n, bool causal, int P_max, int c, int r, int *P_out, int *split_out, int *timed_out,
+                  long long *makespan_out);
+
 }  // namespace dash

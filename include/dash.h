@@ -374,6 +374,20 @@ int dash_choose_schedule(int BH, int n, int causal, int max_ctas, int cost_c, in
 int dash_choose_schedule_split(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
                                int *split_out, long long *makespan_out);
 
+/* The runtime choice over every deterministic layout this library runs (an
+ * extension of dash_choose_schedule_split): each ordered schedule valid for
+ * the mask in its own order, shift or symmetric shift with the split that
+ * dash_choose_split picks, and each of those with timed ranks
+ * (dash_bwd_options_t.rank_order = 1; whole gangs on every SM up to max_ctas,
+ * split gangs on the split's CTA count), by simulated makespan with task costs
+ * C = cost_c and R = cost_r.  Ties keep the lower schedule number, then the
+ * schedule's own order before split gangs before timed ranks.  Writes the CTA
+ * count, the split (1 = whole gangs) and the rank order (0 or 1) to pass as
+ * num_ctas, shift_split and rank_order; returns the schedule, or -1 (with
+ * dash_last_error) when BH, n, max_ctas or a cost is below 1.  Host only. */
+int dash_choose_layout(int BH, int n, int causal, int max_ctas, int cost_c, int cost_r, int *ctas_out,
+                       int *split_out, int *rank_order_out, long long *makespan_out);
+
 /* Task costs for dash_choose_schedule from measured times (the pages' DAG
  * model has a compute cost c and a reduce cost r per task; DASH overview
  * (zskr.cn), section 2.2).  Given the measured backward (or main-kernel)

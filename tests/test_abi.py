@@ -411,3 +411,29 @@ def test_timed_ranks_rejections():
         dash.dash_build_schedule_ex(2, 8, False, "serial", 2, 1, 8)
     assert ei.value.code == 2
 
+
+@pytest.mark.parametrize("BH,n,causal,c,r", [(8, 4, False, 4, 1), (5, 8, False, 4, 1), (6, 8, True, 4, 1),
+                                             (6, 8, True, 1, 3), (16, 16, True, 4, 1), (3, 12, False, 2, 2)])
+def test_layout_choice_is_best_simulated(BH, n, causal, c, r):
+    # every layout priced by the oracle simulator: each ordered schedule in its own order on its chosen CTA count,
+    # the cyclic schedule with the chosen split, and each with timed ranks; ties keep the first candidate
+    P_max = 30
+    cands = []
+    for mode in ("serial", "descending_q", "shift", "symmetric_shift"):
+        if (mode == "shift" and causal) or (mode == "symmetric_shift" and (not causal or n % 2)):
+            continue
+        cyclic = mode in ("shift", "symmetric_shift")
+        P = dash.dash_choose_ctas(BH, n, causal, mode, P_max, c, r)
+        cands.append((d.simulate(d.all_chains(mode, BH, n, causal), P, c, r).makespan, mode, P, 1, 0))
+        k, Pk, _ = dash.dash_choose_split(BH, n, causal, mode, P_max, 0, c, r) if cyclic else (1, 0, 0)
+        if k > 1:
+            cands.append((d.simulate(d.split_chains(mode, BH, n, causal, k), Pk, c, r).makespan, mode, Pk, k, 0))
+        gang = n // 2 if mode == "symmetric_shift" else n
+        Pall = min(P_max, BH * gang)
+        cands.append((d.timed_tables(mode, BH, n, causal, Pall, 1, c, r)[2], mode, Pall, 1, 1))
+        if k > 1:
+            cands.append((d.timed_tables(mode, BH, n, causal, Pk, k, c, r)[2], mode, Pk, k, 1))
+    best = min(cands, key=lambda x: x[0])   # min keeps the first of equal makespans
+    name, P, k, ro, ms = dash.dash_choose_layout(BH, n, causal, P_max, c, r)
+    assert (ms, name, P, k, ro) == best
+

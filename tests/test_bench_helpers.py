@@ -50,6 +50,7 @@ def test_best_label_names_split_gangs_only_when_split():
     assert bench.best_label(det, {"shift": (870.0, 4)}) == "shift+split"
     assert bench.best_label(det, {"shift": (780.0, 1)}) == "shift"     # k = 1 is whole gangs: no label of its own
     assert bench.best_label(det, {}) == "shift"
+    assert bench.best_label(det, {"shift": (870.0, 4)}, {"shift": 880.0}) == "shift+timed"
 
 
 def test_runtime_choice_uses_the_fitted_costs():
@@ -66,3 +67,6 @@ def test_runtime_choice_uses_the_fitted_costs():
     ch = bench.runtime_choice(dash, w, 152, 1.0, 1.45, "shift", "shift+split")
     name, ctas, k, _ = dash.dash_choose_schedule_split(BH, n, w.causal, 152, c, r)
     assert ch["with_split"]["chosen"] == (f"{name}+split" if k > 1 else name) and ch["with_split"]["split"] == k
+    ch = bench.runtime_choice(dash, w, 152, 1.0, 1.45, "shift", "shift+split", "shift+split")
+    name, ctas, k, ro, _ = dash.dash_choose_layout(BH, n, w.causal, 152, c, r)
+    assert ch["layout"]["chosen"] == name + ("+split" if k > 1 else "") + ("+timed" if ro else "")
