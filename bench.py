@@ -425,8 +425,9 @@ def time_other_workload(dash, w, args, flush, stream, world, dev, barrier):
     runs += [(s, 1, 0, 0, split_of(w, s, args.split), 0) for s in ("shift", "symmetric_shift")
              if split_of(w, s, args.split)]
     runs += [(s, 1, 0, 0, 0, 1) for s in ("shift", "symmetric_shift") if s in w.schedules and not args.no_timed]
-    results, _, fill, die, split, timed, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs, args, flush,
-                                                stream, world, dev, barrier)
+    tensors = (q, k, v, o, do, lse, dq, dk, dv)
+    results, _, fill, die, split, timed, launches = time_runs(dash, w, tensors, runs, args, flush, stream, world, dev,
+                                                              barrier)
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
     atomic = results["atomic"]
@@ -516,8 +517,9 @@ def main():
              if s in scheds and split_of(w, s, args.split)]
     runs += [(s, 1, 0, 0, 0, 1) for s in ("shift", "symmetric_shift") if s in scheds and not args.no_timed]
     with ClockSampler(gpu_index) as clk:
-        results, two_chains, fill, die, split, timed, launches = time_runs(dash, w, (q, k, v, o, do, lse, dq, dk, dv), runs,
-                                                             args, flush, stream, world, dev, barrier)
+        tensors = (q, k, v, o, do, lse, dq, dk, dv)
+        results, two_chains, fill, die, split, timed, launches = time_runs(dash, w, tensors, runs, args, flush, stream,
+                                                                           world, dev, barrier)
         also = {}
         for name in [x for x in args.also.split(",") if x and x != w.name]:
             also[name] = time_other_workload(dash, workloads.WORKLOADS[name], args, flush, stream, world, dev,

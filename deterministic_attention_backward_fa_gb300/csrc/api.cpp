@@ -339,17 +339,20 @@ dash_status_t bwd_impl(const void *q, const void *k, const void *v, const void *
                           (mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT);
   const int split = (opt && opt->shift_split > 1) ? opt->shift_split : 1;
   if (split > 1) {
-    if (fill || (opt && opt->tasks)) return fail(DASH_ERR_UNSUPPORTED, "shift_split applies to the library's own table, without fill");
+    if (fill || (opt && opt->tasks))
+      return fail(DASH_ERR_UNSUPPORTED, "shift_split applies to the library's own table, without fill");
     why = dash::check_split(mode, n, split);
     if (!why.empty()) return fail(DASH_ERR_UNSUPPORTED, "%s", why.c_str());
   }
-  if (opt && (opt->rank_order < 0 || opt->rank_order > 1)) return fail(DASH_ERR_INVALID_ARG, "rank_order must be 0 or 1");
+  if (opt && (opt->rank_order < 0 || opt->rank_order > 1))
+    return fail(DASH_ERR_INVALID_ARG, "rank_order must be 0 or 1");
   const bool timed = opt && opt->rank_order == 1 && mode != DASH_SCHED_ATOMIC;
   if (timed && (fill || opt->tasks || opt->die_aware == 1))
     return fail(DASH_ERR_UNSUPPORTED, "rank_order = 1 applies to the library's own table, without fill or die_aware");
   if (opt && (opt->die_aware < 0 || opt->die_aware > 1)) return fail(DASH_ERR_INVALID_ARG, "die_aware must be 0 or 1");
   const bool die_aware = opt && opt->die_aware == 1;
-  if (die_aware && ((mode != DASH_SCHED_SHIFT && mode != DASH_SCHED_SYMMETRIC_SHIFT) || fill || opt->tasks || split > 1))
+  const bool cyclic = mode == DASH_SCHED_SHIFT || mode == DASH_SCHED_SYMMETRIC_SHIFT;
+  if (die_aware && (!cyclic || fill || opt->tasks || split > 1))
     return fail(DASH_ERR_UNSUPPORTED,
                 "die_aware applies to shift and symmetric shift, without fill, split gangs or a supplied table");
   const int want_cluster = opt ? opt->cluster_size : 0;

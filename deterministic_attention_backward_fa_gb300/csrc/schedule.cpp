@@ -721,7 +721,8 @@ int choose_layout(int BH, int n, bool causal, int P_max, int c, int r, int *P_ou
     if (cyclic && k > 1) consider(mode, Pk, k, 0, msk);
     // timed ranks: whole gangs on every SM, and the chosen split's gangs
     const int Pall = (int)std::min<long long>(P_max, (long long)BH * chains_per_head(mode, n));
-    if (build_schedule(BH, n, causal, mode, Pall, c, r, &sch, 1, true).empty()) consider(mode, Pall, 1, 1, sch.makespan);
+    if (build_schedule(BH, n, causal, mode, Pall, c, r, &sch, 1, true).empty())
+      consider(mode, Pall, 1, 1, sch.makespan);
     if (cyclic && k > 1 && build_schedule(BH, n, causal, mode, Pk, c, r, &sch, k, true).empty())
       consider(mode, Pk, k, 1, sch.makespan);
   }
