@@ -249,18 +249,23 @@ def test_timed_ranks_match_oracle(S, D, tile, causal, ctas):
     o, lse = dash.attn_fwd(P.q, P.k, P.v, causal, P.scale)
     q, k, v, do = P.f64
     ref = A.backward(q, k, v, o.double().cpu().numpy(), do, lse.double().cpu().numpy(), causal, P.scale)
+    n = (S + tile - 1) // tile
     for sched in schedules_for(causal, S, tile):
         if sched == "atomic":
             continue
-        for chains in (1, 2):
-            for num in (0, ctas):
-                run = lambda: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile,
-                                            dq_chains=chains, rank_order=1, num_ctas=num)
-                got, again = run(), run()
-                dash.dash_sync_status()
-                for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
-                    assert_close(f"{sched} timed, {chains} chain(s), {num} CTAs {name}", x, r)
-                assert all(torch.equal(a, b) for a, b in zip(got, again))
+        # timed ranks alone, and with split gangs of two where the gang divides
+        gang = n // 2 if sched == "symmetric_shift" else n
+        splits = (1, 2) if sched in ("shift", "symmetric_shift") and gang % 2 == 0 else (1,)
+        for split in splits:
+            for chains in (1, 2):
+                for num in (0, ctas):
+                    run = lambda: dash.attn_bwd(P.q, P.k, P.v, o, P.do, lse, causal, P.scale, sched, tile=tile,
+                                                dq_chains=chains, rank_order=1, num_ctas=num, shift_split=split)
+                    got, again = run(), run()
+                    dash.dash_sync_status()
+                    for name, x, r in zip(("dQ", "dK", "dV"), got, ref):
+                        assert_close(f"{sched} timed split {split}, {chains} chain(s), {num} CTAs {name}", x, r)
+                    assert all(torch.equal(a, b) for a, b in zip(got, again))
 
 
 @pytest.mark.parametrize("wname,sched", [("causal_s16384_d128", "symmetric_shift"), ("full_s4096_d128", "shift")])
@@ -324,10 +329,10 @@ def test_kernel_adds_partials_in_table_rank_order(causal, S, D, tile):
     # the pages' orders, split gangs of two (an extension) for the cyclic schedule, and timed ranks (an
     # extension) of the cyclic schedule on 3 CTAs, which spreads its gangs over time (ranks per head)
     for sched, split, timed in (("serial", 1, 0), ("descending_q", 1, 0), (cyclic, 1, 0), (cyclic, 2, 0),
-                                (cyclic, 1, 1)):
+                                (cyclic, 1, 1), (cyclic, 2, 1)):
         extra = {}
         if timed:
-            tasks_t, _, _ = dash.dash_build_schedule_ex(BH, n, causal, sched, 1, 1, 3)
+            tasks_t, _, _ = dash.dash_build_schedule_ex(BH, n, causal, sched, split, 1, 3)
             rank = {(int(b), int(kv), int(q)): int(w) & dash.TASK_RANK_MASK for b, kv, q, w in tasks_t}
             extra = {"rank_order": 1, "num_ctas": 3}
         else:
