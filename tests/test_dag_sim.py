@@ -278,3 +278,23 @@ def test_timed_ranks_permute_each_tile_and_follow_the_schedule(mode, causal, n, 
     longest = max(len(ch) for _, ch, _ in base)
     assert ordered.makespan <= free.makespan + longest * r * BH
 
+
+@pytest.mark.parametrize("mode,causal", [("serial", False), ("descending_q", False), ("descending_q", True)])
+@pytest.mark.parametrize("n,BH", [(4, 2), (8, 3)])
+def test_timed_ranks_of_serial_and_descending_with_every_chain_at_once(mode, causal, n, BH):
+    # with a CTA per chain every chain starts at time 0; in these schedules all the chains of a head reach a tile
+    # at the same step, so the tie goes to the dispatch position, ascending KV: the pages' order
+    chains = d.all_chains(mode, BH, n, causal)
+    timed = d.timed_chains(chains, len(chains), 4, 1)
+    assert [rk for _, _, rk in timed] == [rk for _, _, rk in chains]
+
+
+@pytest.mark.parametrize("n,BH", [(4, 2), (8, 3)])
+def test_timed_ranks_of_causal_serial_run_in_descending_kv(n, BH):
+    # causal serial: KV j starts at tile j, so with a CTA per chain KV q reaches tile q first and KV 0 last; the
+    # timed order is descending KV, where the pages' order (ascending KV) makes every chain wait on KV 0's
+    chains = d.all_chains("serial", BH, n, True)
+    timed = d.timed_chains(chains, len(chains), 4, 1)
+    for bh, ch, rk in timed:
+        for (kv, q), x in zip(ch, rk):
+            assert x == q - kv
